@@ -1,0 +1,66 @@
+// Plan and workspace layout of the dense prefill stack (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/pds.h"
+
+namespace pds {
+
+struct TmapCache;
+
+enum class Impl { kTensorCore, kNaive };
+
+struct Plan {
+  pds_dims dims{};
+  int q_width = 0, kv_width = 0;
+  Impl impl = Impl::kTensorCore;
+  // Device state made on first use (the device current at that time).
+  int device = -1;
+  int num_sms = 0;
+  uint32_t* d_status = nullptr;  // status word written by bounded device waits
+  TmapCache* maps = nullptr;  // encoded TMA descriptors, reused across calls
+  // Per-kernel timing (pds_plan_set_timing).
+  bool timing = false;
+  struct Mark {
+    int kind;
+    cudaEvent_t start, stop;
+  };
+  std::vector<Mark> marks;          // recorded, not yet read
+  std::vector<cudaEvent_t> events;  // free events
+  int64_t launches[PDS_KERNEL_KINDS] = {};
+  double total_ms[PDS_KERNEL_KINDS] = {};
+};
+
+// Byte offsets into the caller's workspace.
+struct Layout {
+  size_t x, h, a, ss_attn, ss_ffn, q, o, act, rope, c32, gemm_ws, total;
+};
+
+Layout make_layout(const Plan& p, int B);
+
+// Scratch of the tensor-core GEMMs (stream-K partial tiles and tile
+// counters) for a call with batch B.
+size_t gemm_workspace_bytes(const Plan& p, int B);
+
+pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
+                         uint16_t* const* v_cache, int start_pos, int B, const float* x_in,
+                         float* x_out, char* ws, cudaStream_t st, std::string* err);
+
+pds_status plan_sync(Plan& p, cudaStream_t st, std::string* err);
+pds_status plan_kernel_times(Plan& p, cudaStream_t st, pds_kernel_times* out, bool reset,
+                             std::string* err);
+void plan_release_device(Plan& p);
+
+pds_status run_gemm_plain(const uint16_t* A, const uint16_t* W, float* C, int M, int N, int K,
+                          char* ws, size_t ws_bytes, cudaStream_t st, std::string* err);
+pds_status run_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
+                         int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
+                         std::string* err);
+
+}  // namespace pds

@@ -1,0 +1,48 @@
+// Tensor-core (tcgen05 / TMA) kernels of the stack: launch interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/pds.h"
+#include "kernels.h"
+
+namespace pds {
+
+struct TmapCache;  // tensor maps already encoded, keyed by (pointer, shape)
+
+struct TcContext {
+  int num_sms = 0;
+  uint32_t* status = nullptr;  // device status word (bounded waits)
+  char* ws = nullptr;          // GEMM scratch: stream-K partial tiles, tile counters
+  size_t ws_bytes = 0;
+  TmapCache* maps = nullptr;   // optional
+  bool pdl = false;            // launch with programmatic stream serialization
+};
+
+// Largest grid of the persistent GEMM (partial-tile scratch is sized by it).
+constexpr int kGemmMaxGrid = 192;
+
+// Scratch bytes the tensor-core GEMMs need for an M-row problem whose
+// largest GEMM has `max_tiles_n` column tiles.
+size_t tc_gemm_scratch_bytes(int M, int max_tiles_n);
+
+TmapCache* tmap_cache_create();
+void tmap_cache_destroy(TmapCache*);
+
+pds_status tc_gemm_plain(TcContext& c, const uint16_t* A, const uint16_t* W, float* C, int M,
+                         int N, int K, cudaStream_t st, std::string* err);
+pds_status tc_gemm_qkv(TcContext& c, const uint16_t* A, const WeightRows& W, int M, int K,
+                       const QkvEpilogue& e, cudaStream_t st, std::string* err);
+pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int M, int N, int K,
+                         const ResidEpilogue& e, cudaStream_t st, std::string* err);
+pds_status tc_gemm_swiglu(TcContext& c, const uint16_t* A, const WeightRows& W, int M, int K,
+                          const SwigluEpilogue& e, cudaStream_t st, std::string* err);
+pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
+                        std::string* err);
+
+}  // namespace pds

@@ -1,0 +1,232 @@
+/*
+ * pds.h -- C ABI of the GB300 dense prefill stack.
+ *
+ * One call runs a batch of B new tokens through a run of L consecutive
+ * dense Llama-style decoder layers on one GPU and returns the new hidden
+ * batch plus every layer's new K/V rows.  Each layer computes
+ *
+ *     h  = x + wo(attn(rope(q,k), v))      q,k,v = rms_norm(x) . wq/wk/wv
+ *     x' = h + down(silu(gate(m)) * up(m)), m     = rms_norm(h)
+ *
+ * (frink-models 0.49.0 src/fused_layer.rs, module doc "What it refuses":
+ * the fused layer is exactly x + ffn(rms_norm(x + branch)) with a SwiGLU
+ * FFN of one dense expert; frink-models 0.29.0
+ * src/decoder/cuda_prefill.rs, module doc: the hidden batch goes up once
+ * and comes back after the last layer, everything between the seven
+ * matmuls is a kernel, and each layer's K/V rows come back.)
+ *
+ * Conventions for every entry point:
+ *  - Weights are row-major [out, in] bf16 (passed as uint16_t bit
+ *    patterns) and y = x . W^T.  Norm gains are float32 [d].
+ *  - Device pointers must be 16-byte aligned.  The library never frees or
+ *    keeps a caller pointer past the work it enqueues; all work is ordered
+ *    on the caller's stream (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream).
+ *  - Errors: every entry point returns a pds_status.  PDS_DECLINED means
+ *    the call is not one this library serves, decided on the host before
+ *    any device work: nothing was enqueued and no buffer was touched
+ *    (cuda_prefill.rs, try_cuda_prefill_dense_stack: None before
+ *    touching the device or any cache).  PDS_EINVAL is a bad argument.
+ *    PDS_ELAUNCH / PDS_ETIMEOUT are failures after admission: output
+ *    buffers and cache rows [start_pos, start_pos+B) may have been
+ *    written, rows [0, start_pos) never are; the caller must not advance
+ *    its cache length.  The message of the last failure on the calling
+ *    thread is pds_last_error(); each distinct failure message is also
+ *    printed once per process on stderr (cuda_prefill.rs, warn_once).
+ *  - One plan may be used by one stream at a time.
+ */
+#ifndef PDS_H_
+#define PDS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pds_status {
+  PDS_OK = 0,
+  PDS_DECLINED = 1, /* not served; nothing enqueued, nothing touched       */
+  PDS_EINVAL = 2,   /* bad pointer, size, alignment or workspace too small */
+  PDS_ELAUNCH = 3,  /* a CUDA call failed after admission                  */
+  PDS_ETIMEOUT = 4, /* a bounded device-side wait gave up                  */
+  PDS_ENOMEM = 5    /* a host or plan-internal device allocation failed    */
+} pds_status;
+
+/*
+ * Model dimensions of the run (cuda_prefill.rs, PrefillParams: n_heads,
+ * n_kv_heads, head_dim, rms_eps; LayerRopeCuda: theta).  RoPE is the NeoX
+ * layout over the whole head with omega_i = rope_theta^(-2i/head_dim); no
+ * frequency factors, no attention-factor scaling, no softcap, no window;
+ * the attention scale is 1/sqrt(head_dim).  One rms_eps serves both norms.
+ */
+typedef struct pds_dims {
+  int32_t n_layers;   /* L >= 1                                    */
+  int32_t d_model;    /* d: multiple of 128                        */
+  int32_t n_heads;    /* H: multiple of n_kv_heads                 */
+  int32_t n_kv_heads; /* Hkv                                       */
+  int32_t head_dim;   /* hd: 64 or 128; H*hd and Hkv*hd mult. of 128 */
+  int32_t ffn_dim;    /* F: multiple of 128                        */
+  float rope_theta;   /* > 0                                       */
+  float rms_eps;      /* >= 0                                      */
+} pds_dims;
+
+/*
+ * One layer's weights, all device pointers (cuda_prefill.rs,
+ * PrefillDenseLayerCuda: attn_norm_w, ffn_norm_w, q, k, v, o, gate, up,
+ * down).  The caller owns them; they are read, never written.
+ */
+typedef struct pds_layer {
+  const float* attn_norm_w; /* [d]               */
+  const float* ffn_norm_w;  /* [d]               */
+  const uint16_t* wq;       /* [H*hd,   d]  bf16 */
+  const uint16_t* wk;       /* [Hkv*hd, d]  bf16 */
+  const uint16_t* wv;       /* [Hkv*hd, d]  bf16 */
+  const uint16_t* wo;       /* [d, H*hd]    bf16 */
+  const uint16_t* w_gate;   /* [F, d]       bf16 */
+  const uint16_t* w_up;     /* [F, d]       bf16 */
+  const uint16_t* w_down;   /* [d, F]       bf16 */
+} pds_layer;
+
+typedef struct pds_plan pds_plan;
+
+/*
+ * Validate the dimensions and make a plan.  Host only: touches no GPU.
+ * Returns PDS_DECLINED (with *out = NULL) for shapes the kernels do not
+ * serve (see the field comments of pds_dims) or when the environment
+ * variable PDS_DISABLE is set to a non-empty value other than "0"
+ * (cuda_prefill.rs: the cuda_dense_enabled() switch); PDS_EINVAL for a
+ * NULL argument or a non-positive size.  Destroy with pds_plan_destroy.
+ */
+pds_status pds_plan_create(const pds_dims* dims, pds_plan** out);
+
+/* Release a plan and the small device state it made on first use. NULL is a no-op. */
+void pds_plan_destroy(pds_plan* plan);
+
+/*
+ * Bytes of device workspace a call with batch <= max_batch needs.  The
+ * workspace holds the activations between kernels (never the weights or
+ * the caches); its content on entry does not matter.  0 for a NULL plan or
+ * max_batch < 1.
+ */
+size_t pds_workspace_bytes(const pds_plan* plan, int32_t max_batch);
+
+/*
+ * The prefill call, host in / host out (cuda_prefill.rs,
+ * try_cuda_prefill_dense_stack and the launch it makes).
+ *
+ *  layers        host array of n_layers pds_layer (device weight pointers).
+ *  k_cache,
+ *  v_cache       host arrays of n_layers device pointers, each a bf16 cache
+ *                [cache_capacity, n_kv_heads, head_dim].  Rows
+ *                [0, start_pos) hold the prefix (K already rotated) and are
+ *                only read.  On PDS_OK rows [start_pos, start_pos+batch) hold
+ *                this call's new K (post-RoPE) and V rows: these are the
+ *                layer's k_rows / v_rows, row b of the batch at row
+ *                start_pos+b.
+ *  start_pos     s >= 0, the rows already in every cache; new row b is at
+ *                position s+b.
+ *  batch         B >= 1 new tokens; s+B <= cache_capacity.
+ *  hidden_in     host float32 [B, d] (pinned memory makes the copy async
+ *                with respect to other host work, pageable also works).
+ *  hidden_out    host float32 [B, d]; may alias hidden_in.
+ *  workspace     device buffer of >= pds_workspace_bytes(plan, B) bytes.
+ *  stream        cudaStream_t as void*.
+ *
+ * Blocking: returns after the output is in hidden_out (it synchronizes
+ * the stream), so device-side timeouts are reported here as PDS_ETIMEOUT.
+ */
+pds_status pds_prefill_dense_stack(pds_plan* plan, const pds_layer* layers,
+                                   uint16_t* const* k_cache, uint16_t* const* v_cache,
+                                   int32_t cache_capacity, int32_t start_pos, int32_t batch,
+                                   const float* hidden_in, float* hidden_out,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The same call with device input and output (float32 [B, d] each, may
+ * alias), enqueued on the stream without synchronizing.  A device-side
+ * timeout is reported by the next pds_plan_sync (or host-I/O call).
+ */
+pds_status pds_prefill_dense_stack_device(pds_plan* plan, const pds_layer* layers,
+                                          uint16_t* const* k_cache, uint16_t* const* v_cache,
+                                          int32_t cache_capacity, int32_t start_pos,
+                                          int32_t batch, const float* hidden_in_dev,
+                                          float* hidden_out_dev, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronize the stream and report whether any bounded device wait of
+ * this plan's earlier calls gave up (PDS_ETIMEOUT; the flag is then
+ * cleared) or a CUDA error is pending (PDS_ELAUNCH).
+ */
+pds_status pds_plan_sync(pds_plan* plan, void* stream);
+
+/* Message of the last failure on the calling thread ("" if none). Valid until the next call on that thread. */
+const char* pds_last_error(void);
+
+/*
+ * Per-kernel timing (measurement support; no counterpart on the pages).
+ * While enabled, every kernel of the plan's calls is bracketed by CUDA
+ * events recorded on the call's stream, so each kernel's device duration
+ * is measured where it runs.  Off by default (events between kernels cost
+ * a little).  pds_plan_kernel_times synchronizes the stream, adds the
+ * durations of the calls since the last read to the totals and copies the
+ * totals out; reset != 0 clears them afterwards.
+ */
+enum {
+  PDS_KERNEL_PREP = 0,   /* RoPE table + first-layer norm prep, once per call */
+  PDS_KERNEL_QKV = 1,    /* QKV GEMM + norm scale + RoPE + K/V row write      */
+  PDS_KERNEL_ATTN = 2,   /* GQA causal attention                              */
+  PDS_KERNEL_WO = 3,     /* wo GEMM + residual + FFN-norm statistics          */
+  PDS_KERNEL_GATEUP = 4, /* gate/up GEMM + SwiGLU                             */
+  PDS_KERNEL_DOWN = 5,   /* down GEMM + residual + next-norm statistics       */
+  PDS_KERNEL_KINDS = 6
+};
+typedef struct pds_kernel_times {
+  int64_t launches[PDS_KERNEL_KINDS];
+  double total_ms[PDS_KERNEL_KINDS];
+} pds_kernel_times;
+
+pds_status pds_plan_set_timing(pds_plan* plan, int32_t enable);
+pds_status pds_plan_kernel_times(pds_plan* plan, void* stream, pds_kernel_times* out,
+                                 int32_t reset);
+
+/*
+ * Component entry points: the stack's kernels one at a time, on device
+ * buffers, enqueued on the stream (no synchronization).  They serve the
+ * kernel-level tests and take the same shape limits as the stack.
+ */
+
+/*
+ * C[M, N] (float32, row-major, ldc = N) = A[M, K] . W[N, K]^T for bf16 A and
+ * W (row-major, K contiguous).  M >= 1, N multiple of 128, K multiple of
+ * 64.  The same persistent tensor-core GEMM the stack uses, with a plain
+ * store epilogue.  `workspace` (device, >= pds_gemm_workspace_bytes(M, N)
+ * bytes, 16-byte aligned) holds the partial tiles of the k-split and is
+ * written; its content on entry does not matter.
+ */
+pds_status pds_gemm_bf16(const uint16_t* A, const uint16_t* W, float* C, int32_t M, int32_t N,
+                         int32_t K, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Scratch bytes of pds_gemm_bf16 for an M x N output (0 for non-positive sizes). */
+size_t pds_gemm_workspace_bytes(int32_t M, int32_t N);
+
+/*
+ * GQA causal attention of B new query rows over a cache (cuda_prefill.rs,
+ * PrefillParams: prefix_k/prefix_v, start_pos, attn_scale = 1/sqrt(hd)).
+ *  q      bf16 [B, H, hd], already rotated (not pre-scaled).
+ *  k, v   bf16 [>= start_pos+B, Hkv, hd]; rows [0, start_pos+B) are read.
+ *  o      bf16 [B, H*hd]; row b attends rows j <= start_pos + b; query head
+ *         h reads kv head h / (H/Hkv).
+ * Fails with PDS_DECLINED for hd not in {64, 128} or H % Hkv != 0.
+ */
+pds_status pds_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
+                         int32_t batch, int32_t start_pos, int32_t n_heads, int32_t n_kv_heads,
+                         int32_t head_dim, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PDS_H_ */

@@ -1,0 +1,126 @@
+"""The C ABI on the host: the library loads, exports what the header
+declares, and validates/declines before touching any GPU."""
+
+import ctypes
+import os
+
+import pytest
+
+from dense_decoder_layer_gb300 import pds
+
+pytestmark = pytest.mark.skipif(not os.path.exists(pds.LIB_PATH),
+                                reason="libpds.so not built (run __graft_entry__.build())")
+
+
+def _dims(**kw):
+    base = dict(n_layers=2, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn_dim=768,
+                rope_theta=1.0e4, rms_eps=1e-5)
+    base.update(kw)
+    return pds.pds_dims(*[base[f] for f, _ in pds.pds_dims._fields_])
+
+
+def _create(**kw):
+    lib = pds.load()
+    plan = ctypes.c_void_p()
+    st = lib.pds_plan_create(ctypes.byref(_dims(**kw)), ctypes.byref(plan))
+    return st, plan
+
+
+def test_every_declared_function_is_exported():
+    lib = pds.load()
+    names = pds.header_functions()
+    assert "pds_prefill_dense_stack" in names and "pds_plan_create" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_plan_create_accepts_the_served_shapes():
+    for kw in ({}, dict(n_layers=16, d_model=2048, n_heads=32, n_kv_heads=8, ffn_dim=8192),
+               dict(n_layers=28, d_model=3072, n_heads=24, n_kv_heads=8, head_dim=128,
+                    ffn_dim=8192, rope_theta=5e5)):
+        st, plan = _create(**kw)
+        assert st == pds.PDS_OK, pds.last_error()
+        assert pds.pds_workspace_bytes(plan, 512) > 0
+        assert pds.pds_workspace_bytes(plan, 0) == 0
+        pds.pds_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("kw", [dict(head_dim=96), dict(n_heads=5, n_kv_heads=2),
+                                dict(d_model=200), dict(ffn_dim=700),
+                                dict(n_heads=1, n_kv_heads=1, head_dim=64)])
+def test_plan_create_declines_unserved_shapes(kw):
+    st, plan = _create(**kw)
+    assert st == pds.PDS_DECLINED
+    assert not plan.value
+    assert pds.last_error().startswith("declined")
+
+
+@pytest.mark.parametrize("kw", [dict(n_layers=0), dict(d_model=-1), dict(rope_theta=0.0),
+                                dict(rms_eps=-1.0), dict(rms_eps=float("nan"))])
+def test_plan_create_rejects_bad_arguments(kw):
+    st, _ = _create(**kw)
+    assert st == pds.PDS_EINVAL
+
+
+def test_null_arguments():
+    lib = pds.load()
+    assert lib.pds_plan_create(None, None) == pds.PDS_EINVAL
+    lib.pds_plan_destroy(None)
+    assert lib.pds_workspace_bytes(None, 8) == 0
+    assert lib.pds_prefill_dense_stack(None, None, None, None, 0, 0, 1, None, None, None, 0,
+                                       None) == pds.PDS_EINVAL
+
+
+def test_disable_switch_declines(monkeypatch):
+    monkeypatch.setenv("PDS_DISABLE", "1")
+    st, _ = _create()
+    assert st == pds.PDS_DECLINED
+    monkeypatch.setenv("PDS_DISABLE", "0")
+    st, plan = _create()
+    assert st == pds.PDS_OK
+    pds.pds_plan_destroy(plan)
+
+
+def _fake_call(plan, cap, s, B, ws_bytes, device=True, layer_ptr=0x10000, ws=0x20000):
+    """A call whose pointers are never dereferenced: it must be refused on the host."""
+    L = 2
+    layers = (pds.pds_layer * L)()
+    for l in range(L):
+        for f in pds.LAYER_FIELDS:
+            setattr(layers[l], f, layer_ptr)
+    kc = (ctypes.c_void_p * L)(*([0x30000] * L))
+    vc = (ctypes.c_void_p * L)(*([0x40000] * L))
+    fn = pds.load().pds_prefill_dense_stack_device if device else pds.load().pds_prefill_dense_stack
+    return fn(plan, layers, kc, vc, cap, s, B, 0x50000, 0x60000, ws, ws_bytes, None)
+
+
+def test_capacity_overflow_declines_before_any_device_work():
+    st, plan = _create()
+    ws = pds.pds_workspace_bytes(plan, 8)
+    assert _fake_call(plan, cap=16, s=10, B=8, ws_bytes=ws) == pds.PDS_DECLINED
+    assert _fake_call(plan, cap=16, s=10, B=8, ws_bytes=ws, device=False) == pds.PDS_DECLINED
+    pds.pds_plan_destroy(plan)
+
+
+def test_bad_calls_are_invalid():
+    st, plan = _create()
+    ws = pds.pds_workspace_bytes(plan, 8)
+    assert _fake_call(plan, cap=16, s=0, B=0, ws_bytes=ws) == pds.PDS_EINVAL
+    assert _fake_call(plan, cap=16, s=-1, B=8, ws_bytes=ws) == pds.PDS_EINVAL
+    assert _fake_call(plan, cap=16, s=0, B=8, ws_bytes=ws - 1) == pds.PDS_EINVAL
+    assert _fake_call(plan, cap=16, s=0, B=8, ws_bytes=ws, layer_ptr=0x10004) == pds.PDS_EINVAL
+    assert _fake_call(plan, cap=16, s=0, B=8, ws_bytes=ws, ws=0x20008) == pds.PDS_EINVAL
+    assert "16-byte" in pds.last_error()
+    pds.pds_plan_destroy(plan)
+
+
+def test_component_entry_points_validate_on_host():
+    lib = pds.load()
+    assert lib.pds_gemm_bf16(None, None, None, 8, 128, 64, None, 0, None) == pds.PDS_EINVAL
+    assert lib.pds_gemm_bf16(0x100, 0x100, 0x100, 8, 100, 64, 0x100, 1 << 30, None) == pds.PDS_EINVAL
+    assert lib.pds_gemm_bf16(0x100, 0x100, 0x100, 8, 192, 64, 0x100, 1 << 30, None) == pds.PDS_DECLINED
+    assert lib.pds_gemm_bf16(0x100, 0x100, 0x100, 8, 256, 64, 0x100, 16, None) == pds.PDS_EINVAL
+    assert pds.pds_gemm_workspace_bytes(512, 5120) >= pds.pds_gemm_workspace_bytes(8, 128) > 0
+    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 4, 0, 4, 2, 96, None) == pds.PDS_DECLINED
+    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 4, 0, 5, 2, 64, None) == pds.PDS_DECLINED
+    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 0, 0, 4, 2, 64, None) == pds.PDS_EINVAL
