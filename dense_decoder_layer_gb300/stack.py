@@ -14,6 +14,8 @@ import torch
 from . import pds
 
 LAYER_FIELDS = pds.LAYER_FIELDS
+# pds_layer field -> tensor name of a drawn layer (synth.LAYER_TENSORS)
+SYNTH_NAMES = {"attn_norm_w": "attn_norm", "ffn_norm_w": "ffn_norm"}
 
 
 def _bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
@@ -66,7 +68,7 @@ class DenseStack:
         for l in layers:
             t = {}
             for n in LAYER_FIELDS:
-                a = l[n]
+                a = l[n] if n in l else l[SYNTH_NAMES[n]]
                 if a.dtype == np.uint16:
                     t[n] = _bf16_tensor(a, self.device)
                 else:
