@@ -703,4 +703,123 @@ pds_status tc_gemm_qkv(TcContext& c, const uint16_t* A, const WeightRows& W, int
   return launch<128, kEpiQkv>(c, maps, g, st, err);
 }
 
+// ------------------------------------------------ no-allocation GEMM entry
+//
+// Scratch of tc_gemm_plain_noalloc (the C entry pds_gemm_bf16_noalloc): a
+// status word, the stream-K tile counters and the partial tiles, all in
+// one array of this module's global memory, so that the call allocates
+// nothing.  Every GPU that loads the library holds the array until the
+// process exits.  Every call shares it: calls that overlap on one GPU (on
+// any streams) race.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;  // 24 MiB in all
+constexpr size_t kNoAllocStatusBytes = 256;
+constexpr size_t kNoAllocCounterBytes = size_t(64) << 10;  // 16384 tile counters
+constexpr int kNoAllocBN = 128;                            // tiles of 128 x 128
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+char* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the array on the current device.  The name of the
+// array in host code is a host-side stand-in, not a device address: the
+// address is looked up once per device, with that device current.
+pds_status noalloc_scratch(char** out, std::string* err) {
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) {
+    *err = std::string("no CUDA device: ") + cudaGetErrorString(ce);
+    return PDS_ELAUNCH;
+  }
+  if (dev < 0 || dev >= kNoAllocMaxDevices) {
+    *err = "device ordinal beyond the static-scratch table";
+    return PDS_EINVAL;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    ce = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (ce != cudaSuccess || !p) {
+      *err = std::string("static scratch address: ") + cudaGetErrorString(ce);
+      return PDS_ELAUNCH;
+    }
+    g_noalloc_addr[dev] = static_cast<char*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return PDS_OK;
+}
+
+}  // namespace
+
+size_t tc_gemm_noalloc_max_tiles() { return kNoAllocCounterBytes / 4; }
+
+pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Cout, int M, int N,
+                                 int K, int num_sms, cudaStream_t st, std::string* err) {
+  const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * (N / kNoAllocBN);
+  if (tiles > tc_gemm_noalloc_max_tiles()) {
+    *err = "pds_gemm_bf16_noalloc: ceil(M/128) * N/128 = " + std::to_string(tiles) +
+           " output tiles exceed the static scratch's " +
+           std::to_string(tc_gemm_noalloc_max_tiles());
+    return PDS_EINVAL;
+  }
+  char* base = nullptr;
+  pds_status rc = noalloc_scratch(&base, err);
+  if (rc != PDS_OK) return rc;
+  uint32_t* status = reinterpret_cast<uint32_t*>(base);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(base + kNoAllocStatusBytes);
+  float* partials = reinterpret_cast<float*>(base + kNoAllocStatusBytes + kNoAllocCounterBytes);
+  const size_t per_cta = 2 * static_cast<size_t>(BM) * kNoAllocBN * sizeof(float);
+  const int grid_cap = static_cast<int>(
+      (kNoAllocScratchBytes - kNoAllocStatusBytes - kNoAllocCounterBytes) / per_cta);
+
+  // The counters are shared with earlier calls: they must start at zero.
+  cudaError_t ce = cudaMemsetAsync(counters, 0, tiles * 4, st);
+  if (ce != cudaSuccess) {
+    *err = std::string("static scratch counter reset: ") + cudaGetErrorString(ce);
+    return PDS_ELAUNCH;
+  }
+  TcContext c{};
+  c.num_sms = num_sms;
+  GemmMaps maps;
+  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[0], W, K, N, err)) != PDS_OK) return rc;
+  maps.b[1] = maps.b[0];
+  maps.b[2] = maps.b[0];
+  GemmArgs g{};
+  g.wrows0 = N;
+  g.c_out = Cout;
+  g.ldc = N;
+  make_schedule(g, c, M, N / kNoAllocBN, K);
+  g.grid = std::min(g.grid, grid_cap);
+  g.status = status;
+  g.partials = partials;
+  g.counters = counters;
+
+  using Cf = Cfg<kNoAllocBN>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_kernel<kNoAllocBN, kEpiPlain>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(Cf::kSmem));
+  });
+  if (attr_err != cudaSuccess) {
+    *err = std::string("gemm shared-memory attribute: ") + cudaGetErrorString(attr_err);
+    return PDS_ELAUNCH;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g.grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = Cf::kSmem;
+  cfg.stream = st;
+  ce = cudaLaunchKernelEx(&cfg, gemm_kernel<kNoAllocBN, kEpiPlain>, maps, g);
+  if (ce != cudaSuccess) {
+    *err = std::string("gemm launch: ") + cudaGetErrorString(ce);
+    return PDS_ELAUNCH;
+  }
+  return PDS_OK;
+}
+
 }  // namespace pds

@@ -256,6 +256,32 @@ pds_status pds_gemm_bf16(const uint16_t* A, const uint16_t* W, float* C, int32_t
   return PDS_OK;
 }
 
+pds_status pds_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* W, float* C, int32_t M,
+                                 int32_t N, int32_t K, void* stream) {
+  if (!A || !W || !C) return fail(PDS_EINVAL, "pds_gemm_bf16_noalloc: NULL operand");
+  if (M < 1 || N < 128 || K < 64) return fail(PDS_EINVAL, "pds_gemm_bf16_noalloc: bad size");
+  if (N % 128 || K % 64)
+    return fail(PDS_DECLINED,
+                "declined: pds_gemm_bf16_noalloc needs N % 128 == 0 and K % 64 == 0");
+  if (!aligned16(A) || !aligned16(W) || !aligned16(C))
+    return fail(PDS_EINVAL, "pds_gemm_bf16_noalloc: operand not 16-byte aligned");
+  const size_t tiles = static_cast<size_t>((M + 127) / 128) * (N / 128);
+  if (tiles > pds::tc_gemm_noalloc_max_tiles())
+    return fail(PDS_EINVAL, "pds_gemm_bf16_noalloc: ceil(M/128) * (N/128) = " +
+                                std::to_string(tiles) + " output tiles, more than the " +
+                                std::to_string(pds::tc_gemm_noalloc_max_tiles()) +
+                                " its static scratch holds");
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return fail(PDS_ELAUNCH, "pds_gemm_bf16_noalloc: no CUDA device");
+  std::string err;
+  pds_status st = pds::tc_gemm_plain_noalloc(A, W, C, M, N, K, sms,
+                                             static_cast<cudaStream_t>(stream), &err);
+  if (st != PDS_OK) return fail(st, err);
+  return PDS_OK;
+}
+
 pds_status pds_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
                          int32_t batch, int32_t start_pos, int32_t n_heads, int32_t n_kv_heads,
                          int32_t head_dim, void* stream) {

@@ -41,6 +41,12 @@ pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int
                          const ResidEpilogue& e, cudaStream_t st, std::string* err);
 pds_status tc_gemm_swiglu(TcContext& c, const uint16_t* A, const WeightRows& W, int M, int K,
                           const SwigluEpilogue& e, cudaStream_t st, std::string* err);
+// The plain GEMM with its scratch in a static device array instead of a
+// caller buffer (allocates nothing); at most tc_gemm_noalloc_max_tiles()
+// output tiles of 128 x 128.
+size_t tc_gemm_noalloc_max_tiles();
+pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* C, int M, int N,
+                                 int K, int num_sms, cudaStream_t st, std::string* err);
 pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
                         std::string* err);

@@ -79,6 +79,7 @@ def load() -> ctypes.CDLL:
         "pds_last_error": (ctypes.c_char_p, []),
         "pds_gemm_bf16": (st, [vp, vp, vp, i32, i32, i32, vp, sz, vp]),
         "pds_gemm_workspace_bytes": (sz, [i32, i32]),
+        "pds_gemm_bf16_noalloc": (st, [vp, vp, vp, i32, i32, i32, vp]),
         "pds_attention": (st, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "pds_plan_set_timing": (st, [vp, i32]),
         "pds_plan_kernel_times": (st, [vp, vp, ctypes.POINTER(pds_kernel_times), i32]),
@@ -168,6 +169,10 @@ def pds_gemm_workspace_bytes(M: int, N: int) -> int:
 
 def pds_gemm_bf16(A, W, C, M, N, K, workspace, workspace_bytes, stream) -> None:
     check(load().pds_gemm_bf16(A, W, C, M, N, K, workspace, workspace_bytes, stream))
+
+
+def pds_gemm_bf16_noalloc(A, W, C, M, N, K, stream) -> None:
+    check(load().pds_gemm_bf16_noalloc(A, W, C, M, N, K, stream))
 
 
 def pds_attention(q, k, v, o, batch, start_pos, n_heads, n_kv_heads, head_dim, stream) -> None:

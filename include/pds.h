@@ -213,6 +213,32 @@ pds_status pds_gemm_bf16(const uint16_t* A, const uint16_t* W, float* C, int32_t
 size_t pds_gemm_workspace_bytes(int32_t M, int32_t N);
 
 /*
+ * pds_gemm_bf16 for callers that cannot allocate device memory: the same
+ * product, C[M, N] = A[M, K] . W[N, K]^T, with the same operand rules, but
+ * no workspace argument.  The pages have no counterpart; this entry exists
+ * for callers that must not call cudaMalloc -- for example a serving
+ * process whose device memory is all reserved up front by its own pool,
+ * or a plugin that runs inside a host application which owns every
+ * allocation -- and so cannot provide the scratch pds_gemm_bf16 takes.
+ *
+ * The scratch (tile counters and partial tiles of the k-split) lives in a
+ * 24 MiB array of the library's own device memory, which every GPU that
+ * loads the library holds until the process exits.  Limit: at most 16384
+ * output tiles of 128 x 128, i.e. ceil(M/128) * (N/128) <= 16384; larger
+ * sizes return PDS_EINVAL with a message and enqueue nothing.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *
+ * Every call shares the one array and it keeps the last call's contents
+ * (the call clears the counters it needs on its stream): calls that overlap
+ * on the same GPU, on any streams, race -- order them on one stream or
+ * serialize them.  The first call on a device looks up the array's device
+ * address for that device (set-up); make that first call before any
+ * stream capture.
+ */
+pds_status pds_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* W, float* C, int32_t M,
+                                 int32_t N, int32_t K, void* stream);
+
+/*
  * GQA causal attention of B new query rows over a cache (cuda_prefill.rs,
  * PrefillParams: prefix_k/prefix_v, start_pos, attn_scale = 1/sqrt(hd)).
  *  q      bf16 [B, H, hd], already rotated (not pre-scaled).
