@@ -207,9 +207,13 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers (small cases for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     dims = synth.CONFIGS[args.workload]
+    if args.layers:
+        dims = dims.replace(n_layers=args.layers)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

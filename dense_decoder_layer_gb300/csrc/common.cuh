@@ -38,7 +38,7 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // Row scale of RMSNorm from the row's sum-of-squares partials (one per
-// 128-column group of the row, written by the producing epilogue).
+// 64-column group of the row, written by the producing epilogue).
 __device__ __forceinline__ float rms_row_scale(const float* ss_row, int nparts, float inv_d,
                                                float eps) {
   float t = 0.f;

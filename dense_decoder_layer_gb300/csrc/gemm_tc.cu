@@ -2,27 +2,32 @@
 //
 //   C[M, N] = A[M, K] . W[N, K]^T      A, W bf16 (K contiguous), fp32 accumulate
 //
-// One CTA per SM (192 threads, ~193 KB of shared memory, 2*BN TMEM columns):
+// One CTA per SM (320 threads, ~226 KB of shared memory, 2*BN TMEM columns):
 //   warp 0      TMA producer: A box [128 x 64] and W boxes [128 x 64] per
 //               k-block into a ring of S shared-memory stages (128-byte swizzle)
 //   warp 1      tcgen05.mma issuer (one thread): 128 x BN x 16 steps into a
 //               double-buffered TMEM accumulator; commits free the stages
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
-//               output row per thread), fused epilogue, global stores
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               output row; two warps per lane group split the columns),
+//               a warp-private shared-memory transpose, then the fused
+//               epilogue with row-contiguous global loads and stores
 //
-// Work split (stream-K): the tiles x k-blocks iteration space is cut into
-// `grid` equal contiguous ranges, one per CTA.  A tile whose k-blocks are
-// spread over several CTAs is finished by the last of them to arrive: each
+// Work split (grouped stream-K): CTAs form groups of gs (a divisor of the
+// row-tile count, up to 8) that take the same (column tile, k-block) ranges
+// for different row tiles, so the CTAs reading a weight box run in lockstep
+// and the box comes from DRAM once.  The (column tile, k-block) space is cut
+// into equal contiguous ranges, one per group.  A tile whose k-blocks are
+// spread over several groups is finished by the last CTA to arrive: each
 // stores its float32 partial tile to scratch and bumps the tile's counter;
-// the one that sees the final count adds all partials in CTA order (hence
-// in k order: the sum is the same whoever arrives last) and runs the
-// epilogue.  No CTA ever waits for another.
+// the one that sees the final count adds all partials in k order (the sum is
+// the same whoever arrives last) and runs the epilogue.  No CTA ever waits
+// for another.
 //
 // Epilogues (the stack's fusions; frink-models 0.29.0
 // src/decoder/cuda_prefill.rs, module doc: everything between the seven
 // matmuls of a layer is a kernel):
 //   plain   store float32 C
-//   resid   h = resid + acc; store h; a = bf16(h * gain); per-128-column
+//   resid   h = resid + acc; store h; a = bf16(h * gain); per-64-column
 //           sum of squares of h (the next RMSNorm's statistics)
 //   swiglu  act = silu(r*g) * (r*u): W rows of a tile are 128 gate rows then
 //           the same 128 up rows; r = rsqrt(mean sum-of-squares + eps)
@@ -32,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -56,7 +62,13 @@ struct GemmMaps {
 
 struct GemmArgs {
   int M, K;
-  int tiles_m, tiles_n, kb, total, grid;
+  int tiles_m, tiles_n, kb;
+  // Grouped stream-K schedule: a group is `gs` CTAs that take the same
+  // (column tile, k-block) range for `gs` different row tiles, in lockstep,
+  // so a weight box comes from DRAM once and is re-read from L2 while hot.
+  // A unit is (row-tile group mg < mgs, column tile nt); the units x k-blocks
+  // space (`total` iterations) is cut into `groups` equal contiguous ranges.
+  int gs, mgs, units, total, groups, grid;
   int wrows0, wrows1;  // rows of weight blocks 0 and 1 (concatenated along N)
   int pair_mode;       // W tile = 128 rows of block 0 then the same rows of block 1
   uint32_t* status;
@@ -78,15 +90,25 @@ struct Cfg {
   static constexpr uint32_t kStage = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
   static constexpr int kBars = 2 * kStages + 5;
-  static constexpr size_t kSmem = 1024 + kStages * kStage + kBars * 8 + 16;
+  static constexpr uint32_t kMiscBytes = 1024;                  // barriers + misc words
+  static constexpr uint32_t kStageBytes = 8 * 32 * 128;         // epilogue staging, 4 KB a warp
+  static constexpr size_t kSmem = 1024 + kStages * kStage + kMiscBytes + kStageBytes;
+  static_assert(kBars * 8 + 16 <= kMiscBytes, "barrier area");
+  static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-__device__ __forceinline__ int seg_begin(const GemmArgs& g, int c) {
-  return static_cast<int>((static_cast<long long>(c) * g.total) / g.grid);
+// First iteration of group γ's range.
+__device__ __forceinline__ int seg_begin(const GemmArgs& g, int grp) {
+  return static_cast<int>((static_cast<long long>(grp) * g.total) / g.groups);
 }
-// The CTA whose range holds iteration i.
-__device__ __forceinline__ int cta_of_iter(const GemmArgs& g, int i) {
-  return static_cast<int>(((static_cast<long long>(i) + 1) * g.grid - 1) / g.total);
+// The group whose range holds iteration i.
+__device__ __forceinline__ int group_of_iter(const GemmArgs& g, int i) {
+  return static_cast<int>(((static_cast<long long>(i) + 1) * g.groups - 1) / g.total);
+}
+// Row and column tile that CTA rank r of a group computes for unit u.
+__device__ __forceinline__ void unit_tile(const GemmArgs& g, int u, int r, int& mt, int& nt) {
+  nt = u / g.mgs;
+  mt = (u - nt * g.mgs) * g.gs + r;
 }
 
 struct SegIter {
@@ -121,35 +143,79 @@ __device__ __forceinline__ void b_source(const GemmArgs& g, int nt, int h, int& 
   }
 }
 
+// A split tile being finished: contributing groups gf..gl (in k order), this
+// CTA's group `me`, rank `r` within the groups, and the unit.
 struct Fixup {
   bool active;
-  int cf, cl, me, tile;
+  int gf, gl, me, r, unit;
 };
 
-// Chunk j (32 columns) of this thread's accumulator row, plus the partial
-// tiles of the other CTAs of a split tile, summed in CTA order.
+// Warp 0 is the TMA producer, warp 1 the MMA issuer (and TMEM owner).
+// Epilogue threads: warps 2..9.  Warp w reads TMEM lanes 32*(w%4).. (one
+// output row per thread) and takes half of the tile's columns (ch = 0 for
+// warps 2..5, 1 for warps 6..9), so two threads share each row.
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kEpiFirstThread = 64;
+constexpr int kThreads = kEpiFirstThread + kEpiThreads;
+
+// Partial tile of rank r of group grp for unit u: slot 0 if u is the group's
+// first unit (its range starts inside u), else slot 1 (u is its last).
+__device__ __forceinline__ const float4* partial_slot(const GemmArgs& g, int grp, int r, int u,
+                                                      int BN) {
+  const int slot = (seg_begin(g, grp) / g.kb == u) ? 0 : 1;
+  return reinterpret_cast<const float4*>(g.partials) +
+         static_cast<size_t>((grp * g.gs + r) * 2 + slot) * (BM * BN / 4);
+}
+
+// Half h (16 columns) of chunk j of this thread's row: the TMEM
+// accumulator, plus the partial tiles of the other CTAs of a split tile,
+// summed in CTA order (so in k order, whoever reduces).  Two contributors'
+// loads are in flight at once.
 template <int BN>
-__device__ __forceinline__ void load_chunk(const GemmArgs& g, uint32_t taddr, const Fixup& fx,
-                                           int j, int row, float (&v)[32]) {
-  sm100::tmem_load32(taddr + j * 32, v);
-  if (!fx.active) return;
-  float own[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    own[i] = v[i];
-    v[i] = 0.f;
+__device__ __forceinline__ void acc_sub(const GemmArgs& g, uint32_t taddr, const Fixup& fx,
+                                        int j, int h, int row, float (&v)[16]) {
+  if (!fx.active) {
+    sm100::tmem_load16(taddr + j * 32 + h * 16, v);
+    return;
   }
-  for (int c = fx.cf; c <= fx.cl; ++c) {
-    if (c == fx.me) {
+  float own[16];
+  const int q0 = j * 8 + h * 4;
+  for (int c0 = fx.gf; c0 <= fx.gl; c0 += 2) {
+    const int c1 = c0 + 1;
+    const bool has1 = c1 <= fx.gl;
+    const bool ld0 = c0 != fx.me, ld1 = has1 && c1 != fx.me;
+    float4 b0[4], b1[4];
+    // the partial loads go out before the TMEM load, which orders memory
+    if (ld0) {
+      const float4* p = partial_slot(g, c0, fx.r, fx.unit, BN) + q0 * BM + row;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] += own[i];
-    } else {
-      const int slot = (seg_begin(g, c) / g.kb == fx.tile) ? 0 : 1;
-      const float4* p = reinterpret_cast<const float4*>(g.partials) +
-                        static_cast<size_t>(c * 2 + slot) * (BM * BN / 4);
+      for (int q = 0; q < 4; ++q) b0[q] = __ldcg(p + q * BM);
+    }
+    if (ld1) {
+      const float4* p = partial_slot(g, c1, fx.r, fx.unit, BN) + q0 * BM + row;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 x = __ldcg(p + (j * 8 + q) * BM + row);
+      for (int q = 0; q < 4; ++q) b1[q] = __ldcg(p + q * BM);
+    }
+    if (c0 == fx.gf) {
+      sm100::tmem_load16(taddr + j * 32 + h * 16, own);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 x = ld0 ? b0[q] : make_float4(own[4 * q], own[4 * q + 1], own[4 * q + 2],
+                                                 own[4 * q + 3]);
+      v[4 * q] += x.x;
+      v[4 * q + 1] += x.y;
+      v[4 * q + 2] += x.z;
+      v[4 * q + 3] += x.w;
+    }
+    if (has1) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 x = ld1 ? b1[q] : make_float4(own[4 * q], own[4 * q + 1], own[4 * q + 2],
+                                                   own[4 * q + 3]);
         v[4 * q] += x.x;
         v[4 * q + 1] += x.y;
         v[4 * q + 2] += x.z;
@@ -159,150 +225,234 @@ __device__ __forceinline__ void load_chunk(const GemmArgs& g, uint32_t taddr, co
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+// Warp-private staging tile of 32 rows x 128 bytes in shared memory, 16-byte
+// chunks XOR-swizzled by row, so that a thread-per-row write and a
+// four-rows-per-instruction read are both free of bank conflicts.  It turns
+// the TMEM layout (one row per thread) into row-contiguous global accesses.
+struct Stage {
+  float4* base;
+  __device__ __forceinline__ float4& at(int row, int q) const { return base[row * 8 + (q ^ (row & 7))]; }
+};
+
+// 16 float32 of this thread's row into chunks c..c+3 of its staging row.
+__device__ __forceinline__ void stage_f32(const Stage& st, int lane, int c, const float (&v)[16]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                       pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-  }
+  for (int q = 0; q < 4; ++q)
+    st.at(lane, c + q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
+// 16 values of this thread's row as bf16 into chunks c, c+1 of its staging row.
+__device__ __forceinline__ void stage_bf16(const Stage& st, int lane, int c, const float (&v)[16]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    st.at(lane, c + q) = make_float4(__uint_as_float(pack_bf16x2(v[8 * q], v[8 * q + 1])),
+                                     __uint_as_float(pack_bf16x2(v[8 * q + 2], v[8 * q + 3])),
+                                     __uint_as_float(pack_bf16x2(v[8 * q + 4], v[8 * q + 5])),
+                                     __uint_as_float(pack_bf16x2(v[8 * q + 6], v[8 * q + 7])));
+}
+
+// Store staged bf16 chunks c..c+3 (32 columns, 64 bytes) of the warp's rows
+// r < rows to dst_row0 + r * ld, eight rows per instruction.
+__device__ __forceinline__ void flush_bf16(const Stage& st, int c, uint16_t* dst_row0, size_t ld,
+                                           int rows, int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2), q = lane & 3;
+    if (r < rows) *reinterpret_cast<float4*>(dst_row0 + r * ld + q * 8) = st.at(r, c + q);
+  }
+  __syncwarp();
+}
+
+// rsqrt(mean of the row's sum-of-squares partials + eps), loads batched.
+__device__ __forceinline__ float row_scale(const RowScale& rs, int m) {
+  const float* p = rs.ss + static_cast<size_t>(m) * rs.ss_parts;
+  float t = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < rs.ss_parts; ++i) t += p[i];
+  return rsqrtf(t * rs.inv_d + rs.eps);
+}
+
+// The 32-column chunks of the tile this epilogue thread (column half ch) owns.
+template <int BN, int EPI>
+__device__ __forceinline__ int owned_chunk(int ch, int i) {
+  if constexpr (EPI == kEpiSwiglu) {
+    // gate chunks {2ch, 2ch+1} and their up chunks {4+2ch, 5+2ch}
+    return (i < 2) ? 2 * ch + i : 4 + 2 * ch + (i - 2);
+  } else {
+    return ch * (BN / 64) + i;
+  }
+}
+template <int BN, int EPI>
+__host__ __device__ constexpr int owned_chunks() {
+  return EPI == kEpiSwiglu ? 4 : BN / 64;
+}
+template <int BN, int EPI>
+__device__ __forceinline__ bool chunk_exists(const GemmArgs& g, int nt, int j) {
+  if constexpr (EPI == kEpiQkv) return nt * BN + j * 32 < g.qkv.q_width + 2 * g.qkv.kv_width;
+  return true;
+}
+
+// The fused epilogue of one tile for this thread (row `row` of the tile,
+// column half `ch`); r is the row's RMSNorm scale (SwiGLU and QKV).
 template <int BN, int EPI>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, const Fixup& fx,
-                                             int m, int nt, int row) {
+                                             int mt, int nt, int row, int ch, int lane, float r,
+                                             const Stage& st) {
+  const int m = mt * BM + row;
   const bool live = m < g.M;
-  if constexpr (EPI == kEpiPlain) {
-    for (int j = 0; j < BN / 32; ++j) {
-      float v[32];
-      load_chunk<BN>(g, taddr, fx, j, row, v);
-      if (live) {
-        float4* d4 = reinterpret_cast<float4*>(g.c_out + static_cast<size_t>(m) * g.ldc + nt * BN +
-                                               j * 32);
+  const int m0w = mt * BM + (row & ~31);            // first row of this warp's 32
+  const int rows = max(0, min(32, g.M - m0w));      // of which exist
+  if constexpr (EPI == kEpiPlain || EPI == kEpiResid) {
+    const int q = lane & 7;
+    float ss[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    for (int i = 0; i < 8; ++i) ss[i] = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      const int j = ch * (BN / 64) + c;
+      const int n0 = nt * BN + j * 32;
+      // residual and gain in the row-contiguous layout, in flight before the TMEM reads
+      float4 r4[8], g4 = make_float4(1.f, 1.f, 1.f, 1.f);
+      if constexpr (EPI == kEpiResid) {
+        const ResidEpilogue& e = g.resid;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = i * 4 + (lane >> 3);
+          r4[i] = rr < rows ? *reinterpret_cast<const float4*>(
+                                  e.resid + static_cast<size_t>(m0w + rr) * g.resid_n + n0 + 4 * q)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (e.gain) g4 = __ldg(reinterpret_cast<const float4*>(e.gain + n0) + q);
       }
-    }
-  } else if constexpr (EPI == kEpiResid) {
-    const ResidEpilogue& e = g.resid;
-    const int N = g.resid_n;
-    for (int gq = 0; gq < BN / 128; ++gq) {
-      float ss = 0.f;
-      for (int jj = 0; jj < 4; ++jj) {
-        const int j = gq * 4 + jj;
-        const int n = nt * BN + j * 32;
-        float v[32];
-        load_chunk<BN>(g, taddr, fx, j, row, v);
-        if (live) {
-          const size_t off = static_cast<size_t>(m) * N + n;
-          const float4* r4 = reinterpret_cast<const float4*>(e.resid + off);
-          float4* o4 = reinterpret_cast<float4*>(e.out + off);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float4 x = r4[q];
-            x.x += v[4 * q];
-            x.y += v[4 * q + 1];
-            x.z += v[4 * q + 2];
-            x.w += v[4 * q + 3];
-            o4[q] = x;
-            v[4 * q] = x.x;
-            v[4 * q + 1] = x.y;
-            v[4 * q + 2] = x.z;
-            v[4 * q + 3] = x.w;
-          }
+      for (int h = 0; h < 2; ++h) {
+        float v[16];
+        acc_sub<BN>(g, taddr, fx, j, h, row, v);
+        stage_f32(st, lane, 4 * h, v);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = i * 4 + (lane >> 3);
+        const float4 a4 = st.at(rr, q);
+        if constexpr (EPI == kEpiPlain) {
+          if (rr < rows)
+            *reinterpret_cast<float4*>(g.c_out + static_cast<size_t>(m0w + rr) * g.ldc + n0 + 4 * q) = a4;
+        } else {
+          const ResidEpilogue& e = g.resid;
+          const float4 h4 = make_float4(r4[i].x + a4.x, r4[i].y + a4.y, r4[i].z + a4.z, r4[i].w + a4.w);
+          const size_t off = static_cast<size_t>(m0w + rr) * g.resid_n + n0 + 4 * q;
+          if (rr < rows) *reinterpret_cast<float4*>(e.out + off) = h4;
           if (e.gain) {
-            const float4* g4 = reinterpret_cast<const float4*>(e.gain + n);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 gg = g4[q];
-              ss += v[4 * q] * v[4 * q] + v[4 * q + 1] * v[4 * q + 1] +
-                    v[4 * q + 2] * v[4 * q + 2] + v[4 * q + 3] * v[4 * q + 3];
-              v[4 * q] *= gg.x;
-              v[4 * q + 1] *= gg.y;
-              v[4 * q + 2] *= gg.z;
-              v[4 * q + 3] *= gg.w;
-            }
-            store_bf16x32(e.a_out + off, v);
+            if (rr < rows)
+              *reinterpret_cast<uint2*>(e.a_out + off) =
+                  make_uint2(pack_bf16x2(h4.x * g4.x, h4.y * g4.y), pack_bf16x2(h4.z * g4.z, h4.w * g4.w));
+            float s = h4.x * h4.x + h4.y * h4.y + h4.z * h4.z + h4.w * h4.w;
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            ss[i] += s;  // the row's sum over this chunk's 32 columns
           }
         }
       }
-      if (live && e.gain)
-        e.ss_out[static_cast<size_t>(m) * (N / 128) + nt * (BN / 128) + gq] = ss;
+      __syncwarp();
+      if constexpr (EPI == kEpiResid) {
+        const ResidEpilogue& e = g.resid;
+        if (e.gain && (j & 1)) {  // chunks 2k, 2k+1 make a 64-column group of the statistics
+          if (q == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = i * 4 + (lane >> 3);
+              if (rr < rows)
+                e.ss_out[static_cast<size_t>(m0w + rr) * (g.resid_n / 64) + (n0 - 32) / 64] = ss[i];
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ss[i] = 0.f;
+        }
+      }
     }
   } else if constexpr (EPI == kEpiSwiglu) {
     static_assert(BN == 256, "the SwiGLU tile is 128 gate + 128 up columns");
     const SwigluEpilogue& e = g.swiglu;
-    const float r =
-        live ? rms_row_scale(e.rs.ss + static_cast<size_t>(m) * e.rs.ss_parts, e.rs.ss_parts,
-                             e.rs.inv_d, e.rs.eps)
-             : 0.f;
-    for (int jj = 0; jj < 4; ++jj) {
-      float gv[32], uv[32];
-      load_chunk<BN>(g, taddr, fx, jj, row, gv);
-      load_chunk<BN>(g, taddr, fx, 4 + jj, row, uv);
-      if (live) {
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+      const int jg = 2 * ch + i;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) gv[i] = silu(r * gv[i]) * (r * uv[i]);
-        store_bf16x32(e.act + static_cast<size_t>(m) * e.ffn + nt * 128 + jj * 32, gv);
+      for (int h = 0; h < 2; ++h) {
+        float gv[16], uv[16];
+        acc_sub<BN>(g, taddr, fx, jg, h, row, gv);
+        acc_sub<BN>(g, taddr, fx, 4 + jg, h, row, uv);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) gv[k] = silu(r * gv[k]) * (r * uv[k]);
+        stage_bf16(st, lane, 2 * h, gv);
       }
+      flush_bf16(st, 0, e.act + static_cast<size_t>(m0w) * e.ffn + nt * 128 + jg * 32, e.ffn, rows,
+                 lane);
     }
   } else {
+    static_assert(BN == 256, "the QKV tile holds whole heads in each 128-column half");
     const QkvEpilogue& e = g.qkv;
     const int half = e.head_dim / 2;
-    const float r =
-        live ? rms_row_scale(e.rs.ss + static_cast<size_t>(m) * e.rs.ss_parts, e.rs.ss_parts,
-                             e.rs.inv_d, e.rs.eps)
-             : 0.f;
-    for (int hh = 0; hh < BN / 128; ++hh) {
-      const int c0 = nt * BN + hh * 128;
-      if (c0 >= e.q_width + e.kv_width) {
-        uint16_t* dst = e.v_cache + static_cast<size_t>(e.start_pos + m) * e.kv_width +
-                        (c0 - e.q_width - e.kv_width);
-        for (int jj = 0; jj < 4; ++jj) {
-          float v[32];
-          load_chunk<BN>(g, taddr, fx, hh * 4 + jj, row, v);
-          if (live) {
+    const int c0 = nt * BN + ch * 128;  // this thread's 128 columns of [q | k | v]
+    if (c0 >= e.q_width + 2 * e.kv_width) return;
+    if (c0 >= e.q_width + e.kv_width) {
+      uint16_t* dst = e.v_cache + static_cast<size_t>(e.start_pos + m0w) * e.kv_width +
+                      (c0 - e.q_width - e.kv_width);
+#pragma unroll 1
+      for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= r;
-            store_bf16x32(dst + jj * 32, v);
-          }
-        }
-      } else {
-        uint16_t* dst = c0 < e.q_width
-                            ? e.q + static_cast<size_t>(m) * e.q_width + c0
-                            : e.k_cache + static_cast<size_t>(e.start_pos + m) * e.kv_width +
-                                  (c0 - e.q_width);
-        const float2* cs = e.rope + static_cast<size_t>(m) * half;
-        for (int p = 0; p < 2; ++p) {
-          // head_dim 128: one head per 128 columns, pairs (chunk 0, 2) and (1, 3);
-          // head_dim 64: two heads, pairs (0, 1) and (2, 3).
-          const int ja = (e.head_dim == 128) ? p : 2 * p;
-          const int jb = ja + half / 32;
-          const int i0 = (e.head_dim == 128) ? p * 32 : 0;
-          float va[32], vb[32];
-          load_chunk<BN>(g, taddr, fx, hh * 4 + ja, row, va);
-          load_chunk<BN>(g, taddr, fx, hh * 4 + jb, row, vb);
-          if (live) {
+        for (int h = 0; h < 2; ++h) {
+          float v[16];
+          acc_sub<BN>(g, taddr, fx, ch * 4 + jj, h, row, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float2 sc = cs[i0 + i];
-              const float u = r * va[i], w = r * vb[i];
-              va[i] = u * sc.x - w * sc.y;
-              vb[i] = u * sc.y + w * sc.x;
-            }
-            store_bf16x32(dst + ja * 32, va);
-            store_bf16x32(dst + jb * 32, vb);
-          }
+          for (int k = 0; k < 16; ++k) v[k] *= r;
+          stage_bf16(st, lane, 2 * h, v);
         }
+        flush_bf16(st, 0, dst + jj * 32, e.kv_width, rows, lane);
+      }
+    } else {
+      uint16_t* dst = c0 < e.q_width
+                          ? e.q + static_cast<size_t>(m0w) * e.q_width + c0
+                          : e.k_cache + static_cast<size_t>(e.start_pos + m0w) * e.kv_width +
+                                (c0 - e.q_width);
+      const size_t ld = c0 < e.q_width ? e.q_width : e.kv_width;
+      // (cos, sin) table laid out [channel][row]: one channel's rows are contiguous
+      const float2* cs = e.rope + (live ? m : 0);
+#pragma unroll 1
+      for (int p = 0; p < 2; ++p) {
+        // head_dim 128: one head per 128 columns; channel i (< 64) pairs with
+        // i + 64, i.e. chunk p with chunk p + 2.  head_dim 64: two heads, chunk
+        // 2p with chunk 2p + 1.  The rotated halves are staged side by side
+        // (chunks 0-3 and 4-7 of the staging row) and stored together.
+        const int ja = (e.head_dim == 128) ? p : 2 * p;
+        const int jb = ja + half / 32;
+        const int i0 = (e.head_dim == 128) ? p * 32 : 0;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          float va[16], vb[16];
+          acc_sub<BN>(g, taddr, fx, ch * 4 + ja, h, row, va);
+          acc_sub<BN>(g, taddr, fx, ch * 4 + jb, h, row, vb);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 sc = __ldg(cs + static_cast<size_t>(i0 + 16 * h + k) * e.rope_ld);
+            const float u = r * va[k], w = r * vb[k];
+            va[k] = u * sc.x - w * sc.y;
+            vb[k] = u * sc.y + w * sc.x;
+          }
+          stage_bf16(st, lane, 2 * h, va);
+          stage_bf16(st, lane, 4 + 2 * h, vb);
+        }
+        flush_bf16(st, 0, dst + ja * 32, ld, rows, lane);
+        flush_bf16(st, 4, dst + jb * 32, ld, rows, lane);
       }
     }
   }
 }
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g) {
   using namespace sm100;
   using C = Cfg<BN>;
@@ -333,7 +483,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
-      mbar_init(bar_tempty(a), 128);
+      mbar_init(bar_tempty(a), kEpiThreads);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -355,38 +505,63 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem_base = misc[0];
 
   // Everything above overlaps the previous kernel when launched with
-  // programmatic stream serialization; the inputs are only read below.
-  grid_dep_wait();
+  // programmatic stream serialization.  Only the activations (A), the
+  // epilogue's inputs and its outputs depend on that kernel: the producer
+  // starts the weight loads of its first stages before waiting for it, the
+  // epilogue warps wait before they touch global memory, and the MMA warp
+  // only sees shared memory and TMEM.
   grid_dep_launch();
 
-  const int it0 = seg_begin(g, cta), it1 = seg_begin(g, cta + 1);
+  const int grp = cta / g.gs, rank = cta - grp * g.gs;
+  const int it0 = seg_begin(g, grp), it1 = seg_begin(g, grp + 1);
   int issued = 0;  // producer: k-block loads issued
   int consumed = 0;
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+      // A (activations) is re-read by every column tile: keep it; weights
+      // are re-read by the group's row tiles right away: normal priority.
+      const uint64_t pol_w = policy_evict_normal(), pol_a = policy_evict_last();
+      auto load_w = [&](int s, int nt, int kb) {
+#pragma unroll
+        for (int h = 0; h < BN / 128; ++h) {
+          int mi, row;
+          b_source<BN>(g, nt, h, mi, row);
+          tma_load_2d(sbase + s * C::kStage + C::kABytes + h * 16384u, &maps.b[mi], bar_full(s),
+                      kb * BK, row, pol_w);
+        }
+      };
+      const int npre = min(S, it1 - it0);
+      {
+        SegIter pi{it0, it1, g.kb};
+        int unit, k0, k1, n = 0;
+        while (n < npre && pi.next(unit, k0, k1)) {
+          int mt, nt;
+          unit_tile(g, unit, rank, mt, nt);
+          for (int kb = k0; kb < k1 && n < npre; ++kb, ++n) {
+            mbar_arrive_expect_tx(bar_full(n), C::kStage);
+            load_w(n, nt, kb);
+          }
+        }
+      }
+      grid_dep_wait();
       SegIter si{it0, it1, g.kb};
-      int tile, k0, k1;
+      int unit, k0, k1;
       bool ok = true;
-      while (ok && si.next(tile, k0, k1)) {
-        const int mt = tile % g.tiles_m, nt = tile / g.tiles_m;
+      while (ok && si.next(unit, k0, k1)) {
+        int mt, nt;
+        unit_tile(g, unit, rank, mt, nt);
         for (int kb = k0; kb < k1; ++kb) {
           const int s = issued % S;
-          if (!mbar_wait(bar_empty(s), ((issued / S) & 1) ^ 1, abort_flag, g.status)) {
-            ok = false;
-            break;
+          if (issued >= npre) {
+            if (!mbar_wait(bar_empty(s), ((issued / S) & 1) ^ 1, abort_flag, g.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_full(s), C::kStage);
+            load_w(s, nt, kb);
           }
-          const uint32_t dst = sbase + s * C::kStage;
-          mbar_arrive_expect_tx(bar_full(s), C::kStage);
-          tma_load_2d(dst, &maps.a, bar_full(s), kb * BK, mt * BM, pol_a);
-#pragma unroll
-          for (int h = 0; h < BN / 128; ++h) {
-            int mi, row;
-            b_source<BN>(g, nt, h, mi, row);
-            tma_load_2d(dst + C::kABytes + h * 16384u, &maps.b[mi], bar_full(s), kb * BK, row,
-                        pol_w);
-          }
+          tma_load_2d(sbase + s * C::kStage, &maps.a, bar_full(s), kb * BK, mt * BM, pol_a);
           ++issued;
         }
       }
@@ -427,24 +602,42 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(bar_drain, 0, &dummy_abort, g.status);
     }
   } else {
-    const int lane_grp = warp & 3;  // this warp's TMEM lanes: 32*lane_grp ..
+    const Stage st{reinterpret_cast<float4*>(smem + S * C::kStage + C::kMiscBytes) +
+                   (warp - 2) * 256};
+    const int lane_grp = warp & 3;   // this warp's TMEM lanes: 32*lane_grp ..
+    const int ch = (warp - 2) >> 2;  // which half of the tile's columns
     const int row = lane_grp * 32 + lane;
+    const bool leader = threadIdx.x == kEpiFirstThread;
+    grid_dep_wait();
     SegIter si{it0, it1, g.kb};
-    int tile, k0, k1, sg = 0;
-    while (si.next(tile, k0, k1)) {
+    int unit, k0, k1, sg = 0;
+    while (si.next(unit, k0, k1)) {
       const int ab = sg & 1;
+      int mt, nt;
+      unit_tile(g, unit, rank, mt, nt);
+      // the row's RMSNorm scale, read while the accumulator is still being made
+      float rscale = 0.f;
+      if constexpr (EPI == kEpiSwiglu) {
+        if (mt * BM + row < g.M) rscale = row_scale(g.swiglu.rs, mt * BM + row);
+      } else if constexpr (EPI == kEpiQkv) {
+        if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
+      }
       if (!mbar_wait(bar_tfull(ab), (sg >> 1) & 1, abort_flag, g.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_grp * 32) << 16) + ab * BN;
-      const int mt = tile % g.tiles_m, nt = tile / g.tiles_m;
+      const int tile = mt + nt * g.tiles_m;
       const int m = mt * BM + row;
-      Fixup fx{false, 0, 0, cta, tile};
+      Fixup fx{false, 0, 0, grp, rank, unit};
       bool run = true;
       if (!(k0 == 0 && k1 == g.kb)) {
-        const int slot = (it0 / g.kb == tile) ? 0 : 1;
-        float4* mine =
-            reinterpret_cast<float4*>(g.partials) + static_cast<size_t>(cta * 2 + slot) * (BM * BN / 4);
-        for (int j = 0; j < BN / 32; ++j) {
+        const int slot = (it0 / g.kb == unit) ? 0 : 1;
+        float4* mine = reinterpret_cast<float4*>(g.partials) +
+                       static_cast<size_t>(cta * 2 + slot) * (BM * BN / 4);
+        constexpr int kOwned = owned_chunks<BN, EPI>();
+#pragma unroll 1
+        for (int i = 0; i < kOwned; ++i) {
+          const int j = owned_chunk<BN, EPI>(ch, i);
+          if (!chunk_exists<BN, EPI>(g, nt, j)) continue;
           float v[32];
           tmem_load32(taddr + j * 32, v);
 #pragma unroll
@@ -453,21 +646,21 @@ __global__ void __launch_bounds__(192, 1)
                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
         }
         __threadfence();
-        named_bar_sync(1, 128);
-        if (threadIdx.x == 64) misc[1] = atomicAdd(&g.counters[tile], 1u);
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
+        if (leader) misc[1] = atomicAdd(&g.counters[tile], 1u);
+        named_bar_sync(1, kEpiThreads);
         const int arrived = static_cast<int>(misc[1]);
-        const int cf = cta_of_iter(g, tile * g.kb), cl = cta_of_iter(g, tile * g.kb + g.kb - 1);
-        if (arrived == cl - cf) {
+        const int gf = group_of_iter(g, unit * g.kb), gl = group_of_iter(g, unit * g.kb + g.kb - 1);
+        if (arrived == gl - gf) {
           __threadfence();
-          fx = Fixup{true, cf, cl, cta, tile};
+          fx = Fixup{true, gf, gl, grp, rank, unit};
         } else {
           run = false;
         }
       }
       if (run) {
-        run_epilogue<BN, EPI>(g, taddr, fx, m, nt, row);
-        if (fx.active && threadIdx.x == 64) g.counters[tile] = 0;
+        run_epilogue<BN, EPI>(g, taddr, fx, mt, nt, row, ch, lane, rscale, st);
+        if (fx.active && leader) g.counters[tile] = 0;
       }
       tc_fence_before();
       mbar_arrive(bar_tempty(ab));
@@ -475,12 +668,12 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
-  // On a timeout the producer may have loads in flight: let them land
-  // (bounded) before the CTA's shared memory is released.
+  // On a timeout the producer may have loads in flight: give them time to
+  // land (they complete in microseconds) before the shared memory is released.
   if (warp == 0 && lane == 0 && *abort_flag) {
-    int dummy_abort = 0;
-    for (int i = max(0, issued - S); i < issued; ++i)
-      mbar_wait(bar_full(i % S), (i / S) & 1, &dummy_abort, g.status);
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -565,16 +758,50 @@ pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner
   return PDS_OK;
 }
 
-void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K) {
+void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K,
+                   int max_grid = kGemmMaxGrid) {
   g.M = M;
   g.K = K;
   g.tiles_m = (M + BM - 1) / BM;
   g.tiles_n = tiles_n;
   g.kb = K / BK;
-  g.total = g.tiles_m * g.tiles_n * g.kb;
-  int grid = std::min(c.num_sms > 0 ? c.num_sms : 148, kGemmMaxGrid);
-  grid = std::min(grid, std::max(1, g.total / kMinItersPerCta));
-  g.grid = grid;
+  // Group size: all row tiles of a column tile (up to 8), a divisor of tiles_m.
+  int gs = std::min(g.tiles_m, 8);
+  while (g.tiles_m % gs) --gs;
+  g.gs = gs;
+  g.mgs = g.tiles_m / gs;
+  g.units = g.mgs * g.tiles_n;
+  g.total = g.units * g.kb;
+  // PDS_GEMM_CTAS caps the CTAs of every GEMM (a tuning knob; default: one per SM).
+  static const int env_cap = [] {
+    const char* v = std::getenv("PDS_GEMM_CTAS");
+    return v ? std::max(1, std::atoi(v)) : 1 << 30;
+  }();
+  const int ctas = std::min({c.num_sms > 0 ? c.num_sms : 148, kGemmMaxGrid, max_grid, env_cap});
+  const int gmax = std::max(1, std::min(ctas / gs, g.total / kMinItersPerCta));
+  // Pick the group count by a cost model measured on GB300 for these tiles:
+  // about 0.35 us per k-block of a group's range, plus, when units are split
+  // across groups, about 4 us + 5 us per extra contributor for storing,
+  // reducing and re-reading partial tiles.  Fewer CTAs without splits often win.
+  // A single row tile streams every weight byte once: there the bandwidth of
+  // all SMs matters more than splits, so every group is used.
+  double best = 1e30;
+  int best_g = gmax;
+  for (int gr = gmax; g.tiles_m > 1 && gr >= std::max(1, gmax / 3); --gr) {
+    const double per = static_cast<double>(g.total) / gr;
+    double cost = std::ceil(per) * 0.35;
+    if (g.units % gr != 0) {
+      const bool aligned = g.total % gr == 0 && (g.kb % static_cast<int>(per) == 0);
+      const double contrib = g.kb / per + (aligned ? 0.0 : 1.0);
+      cost += 4.0 + 5.0 * std::max(0.0, contrib - 1.0);
+    }
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_g = gr;
+    }
+  }
+  g.groups = best_g;
+  g.grid = g.groups * gs;
 }
 
 template <int BN, int EPI>
@@ -603,7 +830,7 @@ pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t 
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.grid);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cf::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -695,12 +922,10 @@ pds_status tc_gemm_qkv(TcContext& c, const uint16_t* A, const WeightRows& W, int
   g.wrows1 = W.rows[1];
   g.qkv = e;
   const int N = W.rows[0] + W.rows[1] + W.rows[2];
-  if (N % 256 == 0) {
-    make_schedule(g, c, M, N / 256, K);
-    return launch<256, kEpiQkv>(c, maps, g, st, err);
-  }
-  make_schedule(g, c, M, N / 128, K);
-  return launch<128, kEpiQkv>(c, maps, g, st, err);
+  // 256-column tiles always (each 128-column half holds whole heads); a
+  // last half past N reads zero rows and is skipped by the epilogue.
+  make_schedule(g, c, M, (N + 255) / 256, K);
+  return launch<256, kEpiQkv>(c, maps, g, st, err);
 }
 
 // ------------------------------------------------ no-allocation GEMM entry
@@ -791,8 +1016,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   g.wrows0 = N;
   g.c_out = Cout;
   g.ldc = N;
-  make_schedule(g, c, M, N / kNoAllocBN, K);
-  g.grid = std::min(g.grid, grid_cap);
+  make_schedule(g, c, M, N / kNoAllocBN, K, grid_cap);
   g.status = status;
   g.partials = partials;
   g.counters = counters;
@@ -811,7 +1035,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.grid);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cf::kSmem;
   cfg.stream = st;
   ce = cudaLaunchKernelEx(&cfg, gemm_kernel<kNoAllocBN, kEpiPlain>, maps, g);

@@ -16,7 +16,8 @@ struct WeightRows {
 
 // ---- epilogue descriptions (shared by the naive and tensor-core paths) ----
 
-// RMSNorm row scale from sum-of-squares partials [M, ss_parts].
+// RMSNorm row scale from sum-of-squares partials [M, ss_parts], one per
+// 64-column group of the row.
 struct RowScale {
   const float* ss;  // [M, ss_parts]
   int ss_parts;
@@ -29,7 +30,8 @@ struct RowScale {
 // cache rows.
 struct QkvEpilogue {
   RowScale rs;
-  const float2* rope;  // [M, hd/2]
+  const float2* rope;  // [hd/2, rope_ld]: channel i of row b at rope[i * rope_ld + b]
+  int rope_ld;         // row stride of the table (the batch size)
   uint16_t* q;         // [M, H*hd]
   uint16_t* k_cache;   // [cap, Hkv*hd]; row b goes to row start_pos+b
   uint16_t* v_cache;
@@ -38,13 +40,13 @@ struct QkvEpilogue {
 };
 
 // Residual epilogue: out = resid + acc (float32), and for a following
-// norm: a = bf16(out * gain) and per-128-column sum-of-squares partials.
+// norm: a = bf16(out * gain) and per-64-column sum-of-squares partials.
 struct ResidEpilogue {
   const float* resid;  // [M, N]
   float* out;          // [M, N]
   const float* gain;   // [N] or nullptr (no following norm)
   uint16_t* a_out;     // [M, N] bf16
-  float* ss_out;       // [M, N/128]
+  float* ss_out;       // [M, N/64]
 };
 
 // SwiGLU epilogue: act = silu(r*gate) * (r*up), bf16 [M, F].
@@ -56,7 +58,8 @@ struct SwigluEpilogue {
 
 // ---------------------------------------------------------------- launches
 
-// (cos, sin) of pos*omega_i for pos = start_pos + b, b < M, i < hd/2.
+// (cos, sin) of pos*omega_i for pos = start_pos + b, b < M, i < hd/2, laid
+// out [i][b] (table[i * M + b]).
 void launch_rope_table(float2* table, int M, int start_pos, int half, double theta,
                        int head_dim, cudaStream_t st);
 

@@ -68,14 +68,13 @@ __global__ void qkv_epilogue_kernel(const float* __restrict__ C, QkvEpilogue e) 
   const float r = rms_row_scale(e.rs.ss + (size_t)b * e.rs.ss_parts, e.rs.ss_parts, e.rs.inv_d,
                                 e.rs.eps);
   const float* row = C + (size_t)b * N;
-  const float2* cs = e.rope + (size_t)b * half;
   // q and k: rotate the pairs (i, i + hd/2) of every head
   const int n_rot_heads = (e.q_width + e.kv_width) / e.head_dim;
   for (int t = threadIdx.x; t < n_rot_heads * half; t += blockDim.x) {
     const int hh = t / half, i = t % half;
     const int c0 = hh * e.head_dim + i;
     const float u = r * row[c0], w = r * row[c0 + half];
-    const float2 sc = cs[i];
+    const float2 sc = e.rope[(size_t)i * e.rope_ld + b];
     const float o0 = u * sc.x - w * sc.y, o1 = u * sc.y + w * sc.x;
     uint16_t* dst;
     if (c0 < e.q_width) {
@@ -92,19 +91,19 @@ __global__ void qkv_epilogue_kernel(const float* __restrict__ C, QkvEpilogue e) 
   }
 }
 
-// One CTA (8 warps) per row; a warp per 128-column group.
+// One CTA (8 warps) per row; a warp per 64-column group of the statistics.
 __global__ void resid_epilogue_kernel(const float* __restrict__ C, ResidEpilogue e, int N) {
   const int b = blockIdx.x;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int groups = N / 128;
+  const int groups = N / 64;
   for (int gi = warp; gi < groups; gi += blockDim.x / 32) {
     float ss = 0.f;
-    for (int j = lane; j < 128; j += 32) {
-      const size_t idx = (size_t)b * N + gi * 128 + j;
+    for (int j = lane; j < 64; j += 32) {
+      const size_t idx = (size_t)b * N + gi * 64 + j;
       float hv = e.resid[idx] + (C ? C[idx] : 0.f);
       if (e.out) e.out[idx] = hv;
       if (e.gain) {
-        e.a_out[idx] = f32_to_bf16(hv * e.gain[gi * 128 + j]);
+        e.a_out[idx] = f32_to_bf16(hv * e.gain[gi * 64 + j]);
         ss += hv * hv;
       }
     }
@@ -179,7 +178,7 @@ __global__ void rope_table_kernel(float2* table, int M, int start_pos, int half,
                                   int head_dim) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= M * half) return;
-  const int b = t / half, i = t % half;
+  const int i = t / M, b = t % M;  // table laid out [channel][row]
   const double omega = pow(theta, -2.0 * i / head_dim);
   double s, c;
   sincos((double)(start_pos + b) * omega, &s, &c);

@@ -68,8 +68,8 @@ Layout make_layout(const Plan& p, int B) {
   L.x = take(Bz * d * 4);
   L.h = take(Bz * d * 4);
   L.a = take(Bz * d * 2);
-  L.ss_attn = take(Bz * (d / 128) * 4);
-  L.ss_ffn = take(Bz * (d / 128) * 4);
+  L.ss_attn = take(Bz * (d / 64) * 4);
+  L.ss_ffn = take(Bz * (d / 64) * 4);
   L.q = take(Bz * p.q_width * 2);
   L.o = take(Bz * p.q_width * 2);
   L.act = take(Bz * p.dims.ffn_dim * 2);
@@ -123,6 +123,10 @@ pds_status pds_plan_create(const pds_dims* dims, pds_plan** out) {
   p->kv_width = d.n_kv_heads * d.head_dim;
   const char* impl = std::getenv("PDS_KERNELS");
   p->impl = (impl && std::strcmp(impl, "naive") == 0) ? Impl::kNaive : Impl::kTensorCore;
+  const char* g = std::getenv("PDS_GRAPH");
+  p->graphs = !(g && std::strcmp(g, "0") == 0);
+  const char* pdl = std::getenv("PDS_PDL");
+  p->pdl = !(pdl && std::strcmp(pdl, "0") == 0);
   *out = p;
   return PDS_OK;
 }
@@ -178,7 +182,7 @@ pds_status pds_prefill_dense_stack_device(pds_plan* plan, const pds_layer* layer
                              hidden_in_dev, hidden_out_dev, workspace, workspace_bytes, true);
   if (st != PDS_OK) return st;
   std::string err;
-  st = pds::enqueue_stack(*plan, layers, k_cache, v_cache, start_pos, batch, hidden_in_dev,
+  st = pds::run_stack(*plan, layers, k_cache, v_cache, start_pos, batch, hidden_in_dev,
                           hidden_out_dev, static_cast<char*>(workspace),
                           static_cast<cudaStream_t>(stream), &err);
   if (st != PDS_OK) return fail(st, err);
@@ -201,7 +205,7 @@ pds_status pds_prefill_dense_stack(pds_plan* plan, const pds_layer* layers,
   if (ce != cudaSuccess)
     return fail(PDS_ELAUNCH, std::string("upload of hidden_in: ") + cudaGetErrorString(ce));
   std::string err;
-  st = pds::enqueue_stack(*plan, layers, k_cache, v_cache, start_pos, batch, xdev, xdev,
+  st = pds::run_stack(*plan, layers, k_cache, v_cache, start_pos, batch, xdev, xdev,
                           static_cast<char*>(workspace), s, &err);
   if (st != PDS_OK) return fail(st, err);
   ce = cudaMemcpyAsync(hidden_out, xdev, bytes, cudaMemcpyDeviceToHost, s);

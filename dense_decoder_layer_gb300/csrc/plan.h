@@ -35,6 +35,19 @@ struct Plan {
   std::vector<cudaEvent_t> events;  // free events
   int64_t launches[PDS_KERNEL_KINDS] = {};
   double total_ms[PDS_KERNEL_KINDS] = {};
+  // CUDA graphs of recent call shapes: the whole call (every kernel of every
+  // layer) is captured once per key (all pointers, start_pos, batch) and
+  // replayed.  PDS_GRAPH=0 turns this off.
+  bool graphs = true;
+  bool pdl = true;  // programmatic dependent launch between GEMMs (PDS_PDL=0 off)
+  struct Graph {
+    std::vector<uintptr_t> key;
+    cudaGraphExec_t exec = nullptr;
+    uint64_t last_use = 0;
+  };
+  std::vector<Graph> graph_cache;
+  uint64_t graph_clock = 0;
+  cudaStream_t capture_stream = nullptr;
 };
 
 // Byte offsets into the caller's workspace.
@@ -51,6 +64,11 @@ size_t gemm_workspace_bytes(const Plan& p, int B);
 pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
                          uint16_t* const* v_cache, int start_pos, int B, const float* x_in,
                          float* x_out, char* ws, cudaStream_t st, std::string* err);
+
+// enqueue_stack through the plan's graph cache (or directly when graphs are off).
+pds_status run_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
+                     uint16_t* const* v_cache, int start_pos, int B, const float* x_in,
+                     float* x_out, char* ws, cudaStream_t st, std::string* err);
 
 pds_status plan_sync(Plan& p, cudaStream_t st, std::string* err);
 pds_status plan_kernel_times(Plan& p, cudaStream_t st, pds_kernel_times* out, bool reset,

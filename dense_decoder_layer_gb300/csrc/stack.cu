@@ -89,6 +89,11 @@ size_t gemm_workspace_bytes(const Plan& p, int B) {
 }
 
 void plan_release_device(Plan& p) {
+  for (Plan::Graph& g : p.graph_cache)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  p.graph_cache.clear();
+  if (p.capture_stream) cudaStreamDestroy(p.capture_stream);
+  p.capture_stream = nullptr;
   for (const Plan::Mark& m : p.marks) {
     cudaEventDestroy(m.start);
     cudaEventDestroy(m.stop);
@@ -144,7 +149,7 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
   uint16_t* O = reinterpret_cast<uint16_t*>(ws + lay.o);
   uint16_t* ACT = reinterpret_cast<uint16_t*>(ws + lay.act);
   float2* rope = reinterpret_cast<float2*>(ws + lay.rope);
-  const int parts = d / 128;
+  const int parts = d / 64;
   const float inv_d = 1.0f / (float)d;
 
   // Per-kernel timing marks (pds_plan_set_timing): events on the call's stream.
@@ -180,7 +185,7 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
     tc.ws = ws + lay.gemm_ws;
     tc.ws_bytes = gemm_workspace_bytes(p, B);
     tc.maps = p.maps;
-    tc.pdl = false;
+    tc.pdl = p.pdl;
     // stream-K tile counters start at zero; every GEMM leaves them at zero
     const size_t part = tc_gemm_scratch_bytes(B, 0);
     cudaError_t ce = cudaMemsetAsync(tc.ws + part, 0, tc.ws_bytes - part, st);
@@ -199,6 +204,7 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
     QkvEpilogue qe{};
     qe.rs = RowScale{ss_attn, parts, inv_d, D.rms_eps};
     qe.rope = rope;
+    qe.rope_ld = B;
     qe.q = Q;
     qe.k_cache = k_cache[l];
     qe.v_cache = v_cache[l];
@@ -261,6 +267,80 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
       done(mk);
       if (rc != PDS_OK) return rc;
     }
+  }
+  return PDS_OK;
+}
+
+pds_status run_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
+                     uint16_t* const* v_cache, int s, int B, const float* x_in, float* x_out,
+                     char* ws, cudaStream_t st, std::string* err) {
+  if (!p.graphs || p.timing)
+    return enqueue_stack(p, layers, k_cache, v_cache, s, B, x_in, x_out, ws, st, err);
+  pds_status rc = ensure_device_state(p, err);
+  if (rc != PDS_OK) return rc;
+  std::vector<uintptr_t> key;
+  key.reserve(8 + 11 * p.dims.n_layers);
+  key.push_back(static_cast<uintptr_t>(s));
+  key.push_back(static_cast<uintptr_t>(B));
+  key.push_back(reinterpret_cast<uintptr_t>(x_in));
+  key.push_back(reinterpret_cast<uintptr_t>(x_out));
+  key.push_back(reinterpret_cast<uintptr_t>(ws));
+  for (int l = 0; l < p.dims.n_layers; ++l) {
+    const pds_layer& w = layers[l];
+    for (const void* q : {(const void*)w.attn_norm_w, (const void*)w.ffn_norm_w,
+                          (const void*)w.wq, (const void*)w.wk, (const void*)w.wv,
+                          (const void*)w.wo, (const void*)w.w_gate, (const void*)w.w_up,
+                          (const void*)w.w_down, (const void*)k_cache[l], (const void*)v_cache[l]})
+      key.push_back(reinterpret_cast<uintptr_t>(q));
+  }
+  Plan::Graph* hit = nullptr;
+  for (Plan::Graph& g : p.graph_cache)
+    if (g.key == key) hit = &g;
+  if (!hit) {
+    cudaError_t ce = cudaSuccess;
+    if (!p.capture_stream) ce = cudaStreamCreateWithFlags(&p.capture_stream, cudaStreamNonBlocking);
+    if (ce == cudaSuccess)
+      ce = cudaStreamBeginCapture(p.capture_stream, cudaStreamCaptureModeRelaxed);
+    if (ce != cudaSuccess) {
+      *err = std::string("graph capture start: ") + cudaGetErrorString(ce);
+      return PDS_ELAUNCH;
+    }
+    rc = enqueue_stack(p, layers, k_cache, v_cache, s, B, x_in, x_out, ws, p.capture_stream, err);
+    cudaGraph_t graph = nullptr;
+    ce = cudaStreamEndCapture(p.capture_stream, &graph);
+    if (rc != PDS_OK || ce != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      if (rc == PDS_OK) {
+        *err = std::string("graph capture: ") + cudaGetErrorString(ce);
+        rc = PDS_ELAUNCH;
+      }
+      cudaGetLastError();
+      return rc;
+    }
+    cudaGraphExec_t exec = nullptr;
+    ce = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ce != cudaSuccess) {
+      *err = std::string("graph instantiate: ") + cudaGetErrorString(ce);
+      return PDS_ELAUNCH;
+    }
+    constexpr size_t kMaxGraphs = 4;
+    if (p.graph_cache.size() >= kMaxGraphs) {
+      auto lru = std::min_element(p.graph_cache.begin(), p.graph_cache.end(),
+                                  [](const Plan::Graph& a, const Plan::Graph& b) {
+                                    return a.last_use < b.last_use;
+                                  });
+      cudaGraphExecDestroy(lru->exec);
+      p.graph_cache.erase(lru);
+    }
+    p.graph_cache.push_back(Plan::Graph{std::move(key), exec, 0});
+    hit = &p.graph_cache.back();
+  }
+  hit->last_use = ++p.graph_clock;
+  cudaError_t ce = cudaGraphLaunch(hit->exec, st);
+  if (ce != cudaSuccess) {
+    *err = std::string("graph launch: ") + cudaGetErrorString(ce);
+    return PDS_ELAUNCH;
   }
   return PDS_OK;
 }

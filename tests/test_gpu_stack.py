@@ -17,6 +17,9 @@ RAGGED = {
     "ragged-hd64": synth.Dims(2, 512, 8, 2, 64, 1536, 130, 70, 1.0e4),
     "ragged-hd128": synth.Dims(3, 768, 6, 2, 128, 2048, 200, 37, 5.0e5),
     "single-row": synth.Dims(2, 256, 4, 2, 64, 768, 1, 5, 1.0e4),
+    # q|k|v = 384+128+128 columns: the last 256-column QKV tile is half empty;
+    # d = 384 takes the 128-column residual tiles
+    "odd-heads": synth.Dims(2, 384, 3, 1, 128, 768, 77, 9, 1.0e4),
 }
 
 
@@ -28,7 +31,7 @@ def _check(got, want, tag):
 
 
 @pytest.mark.parametrize("impl", ["tc", "naive"])
-@pytest.mark.parametrize("name", ["tiny", "ragged-hd64", "ragged-hd128", "single-row"])
+@pytest.mark.parametrize("name", ["tiny", "ragged-hd64", "ragged-hd128", "single-row", "odd-heads"])
 def test_small_stacks_match_oracle(name, impl):
     dims = RAGGED.get(name) or synth.CONFIGS[name]
     dims, (layers, pk, pv, hidden) = workload(dims)
