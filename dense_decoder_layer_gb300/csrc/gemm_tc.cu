@@ -49,6 +49,12 @@ namespace pds {
 
 namespace {
 
+// Phase hooks for timing studies: a build may define PDS_GEMM_TRACE_HOOK(cta,
+// point) to record when each CTA reaches a point; by default they vanish.
+#ifndef PDS_GEMM_TRACE_HOOK
+#define PDS_GEMM_TRACE_HOOK(cta, point) ((void)0)
+#endif
+
 enum EpiKind { kEpiPlain = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiQkv = 3 };
 
 constexpr int BM = 128;
@@ -69,6 +75,9 @@ struct GemmArgs {
   // A unit is (row-tile group mg < mgs, column tile nt); the units x k-blocks
   // space (`total` iterations) is cut into `groups` equal contiguous ranges.
   int gs, mgs, units, total, groups, grid;
+  // The CTAs of a group run as clusters of cs (1, 2 or 4): each loads 1/cs
+  // of the shared weight tile and multicasts it to the whole cluster.
+  int cs;
   int wrows0, wrows1;  // rows of weight blocks 0 and 1 (concatenated along N)
   int pair_mode;       // W tile = 128 rows of block 0 then the same rows of block 1
   uint32_t* status;
@@ -229,6 +238,20 @@ __device__ __forceinline__ void acc_sub(const GemmArgs& g, uint32_t taddr, const
 // chunks XOR-swizzled by row, so that a thread-per-row write and a
 // four-rows-per-instruction read are both free of bank conflicts.  It turns
 // the TMEM layout (one row per thread) into row-contiguous global accesses.
+// Two 16-column pieces (chunk ja half ha, chunk jb half hb) of this thread's
+// row; without a split the two TMEM loads share one wait.
+template <int BN>
+__device__ __forceinline__ void acc_pair(const GemmArgs& g, uint32_t taddr, const Fixup& fx,
+                                         int ja, int ha, int jb, int hb, int row, float (&va)[16],
+                                         float (&vb)[16]) {
+  if (!fx.active) {
+    sm100::tmem_load16x2(taddr + ja * 32 + ha * 16, taddr + jb * 32 + hb * 16, va, vb);
+    return;
+  }
+  acc_sub<BN>(g, taddr, fx, ja, ha, row, va);
+  acc_sub<BN>(g, taddr, fx, jb, hb, row, vb);
+}
+
 struct Stage {
   float4* base;
   __device__ __forceinline__ float4& at(int row, int q) const { return base[row * 8 + (q ^ (row & 7))]; }
@@ -255,11 +278,15 @@ __device__ __forceinline__ void stage_bf16(const Stage& st, int lane, int c, con
 // r < rows to dst_row0 + r * ld, eight rows per instruction.
 __device__ __forceinline__ void flush_bf16(const Stage& st, int c, uint16_t* dst_row0, size_t ld,
                                            int rows, int lane) {
+  // activations are read again soon: keep them in L2 while weights stream by
+  const uint64_t pol = sm100::policy_evict_last();
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = i * 8 + (lane >> 2), q = lane & 3;
-    if (r < rows) *reinterpret_cast<float4*>(dst_row0 + r * ld + q * 8) = st.at(r, c + q);
+    if (r < rows)
+      sm100::st_global_hint(reinterpret_cast<float4*>(dst_row0 + r * ld + q * 8), st.at(r, c + q),
+                            pol);
   }
   __syncwarp();
 }
@@ -305,6 +332,9 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
   const int rows = max(0, min(32, g.M - m0w));      // of which exist
   if constexpr (EPI == kEpiPlain || EPI == kEpiResid) {
     const int q = lane & 7;
+    // the residual stream and the next GEMM's operand are read again within
+    // the layer: keep them in L2 while the weights stream by
+    const uint64_t pol_keep = sm100::policy_evict_last();
     float ss[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) ss[i] = 0.f;
@@ -325,11 +355,11 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
         }
         if (e.gain) g4 = __ldg(reinterpret_cast<const float4*>(e.gain + n0) + q);
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float v[16];
-        acc_sub<BN>(g, taddr, fx, j, h, row, v);
-        stage_f32(st, lane, 4 * h, v);
+      {
+        float v0[16], v1[16];
+        acc_pair<BN>(g, taddr, fx, j, 0, j, 1, row, v0, v1);
+        stage_f32(st, lane, 0, v0);
+        stage_f32(st, lane, 4, v1);
       }
       __syncwarp();
 #pragma unroll
@@ -343,11 +373,13 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
           const ResidEpilogue& e = g.resid;
           const float4 h4 = make_float4(r4[i].x + a4.x, r4[i].y + a4.y, r4[i].z + a4.z, r4[i].w + a4.w);
           const size_t off = static_cast<size_t>(m0w + rr) * g.resid_n + n0 + 4 * q;
-          if (rr < rows) *reinterpret_cast<float4*>(e.out + off) = h4;
+          if (rr < rows) sm100::st_global_hint(reinterpret_cast<float4*>(e.out + off), h4, pol_keep);
           if (e.gain) {
             if (rr < rows)
-              *reinterpret_cast<uint2*>(e.a_out + off) =
-                  make_uint2(pack_bf16x2(h4.x * g4.x, h4.y * g4.y), pack_bf16x2(h4.z * g4.z, h4.w * g4.w));
+              sm100::st_global_hint(
+                  reinterpret_cast<uint2*>(e.a_out + off),
+                  make_uint2(pack_bf16x2(h4.x * g4.x, h4.y * g4.y), pack_bf16x2(h4.z * g4.z, h4.w * g4.w)),
+                  pol_keep);
             float s = h4.x * h4.x + h4.y * h4.y + h4.z * h4.z + h4.w * h4.w;
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
@@ -382,8 +414,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float gv[16], uv[16];
-        acc_sub<BN>(g, taddr, fx, jg, h, row, gv);
-        acc_sub<BN>(g, taddr, fx, 4 + jg, h, row, uv);
+        acc_pair<BN>(g, taddr, fx, jg, h, 4 + jg, h, row, gv, uv);
 #pragma unroll
         for (int k = 0; k < 16; ++k) gv[k] = silu(r * gv[k]) * (r * uv[k]);
         stage_bf16(st, lane, 2 * h, gv);
@@ -402,14 +433,15 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
                       (c0 - e.q_width - e.kv_width);
 #pragma unroll 1
       for (int jj = 0; jj < 4; ++jj) {
+        float v0[16], v1[16];
+        acc_pair<BN>(g, taddr, fx, ch * 4 + jj, 0, ch * 4 + jj, 1, row, v0, v1);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float v[16];
-          acc_sub<BN>(g, taddr, fx, ch * 4 + jj, h, row, v);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] *= r;
-          stage_bf16(st, lane, 2 * h, v);
+        for (int k = 0; k < 16; ++k) {
+          v0[k] *= r;
+          v1[k] *= r;
         }
+        stage_bf16(st, lane, 0, v0);
+        stage_bf16(st, lane, 2, v1);
         flush_bf16(st, 0, dst + jj * 32, e.kv_width, rows, lane);
       }
     } else {
@@ -432,8 +464,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           float va[16], vb[16];
-          acc_sub<BN>(g, taddr, fx, ch * 4 + ja, h, row, va);
-          acc_sub<BN>(g, taddr, fx, ch * 4 + jb, h, row, vb);
+          acc_pair<BN>(g, taddr, fx, ch * 4 + ja, h, ch * 4 + jb, h, row, va, vb);
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const float2 sc = __ldg(cs + static_cast<size_t>(i0 + 16 * h + k) * e.rope_ld);
@@ -479,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_empty(s), g.cs);  // freed by the MMAs of every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
@@ -502,7 +533,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // peers multicast into this CTA's stages and arrive on its barriers
+  if (g.cs > 1) cluster_sync();
   const uint32_t tmem_base = misc[0];
+  const uint16_t cmask = static_cast<uint16_t>((1u << g.cs) - 1);
+  if (threadIdx.x == 0) PDS_GEMM_TRACE_HOOK(cta, 0);
 
   // Everything above overlaps the previous kernel when launched with
   // programmatic stream serialization.  Only the activations (A), the
@@ -519,16 +554,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // A (activations) is re-read by every column tile: keep it; weights
-      // are re-read by the group's row tiles right away: normal priority.
-      const uint64_t pol_w = policy_evict_normal(), pol_a = policy_evict_last();
+      // A (activations) is re-read by every column tile: keep it.  A weight
+      // box is read once when one cluster holds all the row tiles of its
+      // group (it is multicast to them): let it go first; otherwise the
+      // group's other clusters read it again right away: normal priority.
+      const uint64_t pol_a = policy_evict_last();
+      const uint64_t pol_w = g.cs == g.gs ? policy_evict_first() : policy_evict_normal();
+      const int slice = BN / g.cs;  // weight rows this CTA loads for the cluster
+      const int r0 = (g.cs > 1 ? static_cast<int>(cluster_rank()) : 0) * slice;
       auto load_w = [&](int s, int nt, int kb) {
+        if (g.cs == 1) {
 #pragma unroll
-        for (int h = 0; h < BN / 128; ++h) {
+          for (int h = 0; h < BN / 128; ++h) {
+            int mi, row;
+            b_source<BN>(g, nt, h, mi, row);
+            tma_load_2d(sbase + s * C::kStage + C::kABytes + h * 16384u, &maps.b[mi], bar_full(s),
+                        kb * BK, row, pol_w);
+          }
+        } else {
           int mi, row;
-          b_source<BN>(g, nt, h, mi, row);
-          tma_load_2d(sbase + s * C::kStage + C::kABytes + h * 16384u, &maps.b[mi], bar_full(s),
-                      kb * BK, row, pol_w);
+          b_source<BN>(g, nt, r0 / 128, mi, row);
+          tma_load_2d_mc(sbase + s * C::kStage + C::kABytes + r0 * 128u, &maps.b[mi], bar_full(s),
+                         kb * BK, row + (r0 % 128), cmask, pol_w);
         }
       };
       const int npre = min(S, it1 - it0);
@@ -545,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       grid_dep_wait();
+      PDS_GEMM_TRACE_HOOK(cta, 1);
       SegIter si{it0, it1, g.kb};
       int unit, k0, k1;
       bool ok = true;
@@ -583,17 +631,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          if (consumed == 0) PDS_GEMM_TRACE_HOOK(cta, 2);
           const uint32_t a_addr = sbase + s * C::kStage;
           const uint64_t ad = smem_desc_sw128(a_addr);
           const uint64_t bd = smem_desc_sw128(a_addr + C::kABytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, (kb > k0 || k > 0) ? 1u : 0u);
-          umma_commit(bar_empty(s));
+          if (g.cs > 1) {
+            umma_commit_mc(bar_empty(s), cmask);  // the stage is free in every CTA's view
+          } else {
+            umma_commit(bar_empty(s));
+          }
           ++consumed;
         }
         if (!ok) break;
         umma_commit(bar_tfull(ab));
+        PDS_GEMM_TRACE_HOOK(cta, 3);
         ++sg;
       }
       // Every MMA this thread issued has completed before TMEM is released.
@@ -624,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!mbar_wait(bar_tfull(ab), (sg >> 1) & 1, abort_flag, g.status)) break;
       tc_fence_after();
+      if (leader) PDS_GEMM_TRACE_HOOK(cta, 4);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_grp * 32) << 16) + ab * BN;
       const int tile = mt + nt * g.tiles_m;
       const int m = mt * BM + row;
@@ -662,6 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         run_epilogue<BN, EPI>(g, taddr, fx, mt, nt, row, ch, lane, rscale, st);
         if (fx.active && leader) g.counters[tile] = 0;
       }
+      if (leader) PDS_GEMM_TRACE_HOOK(cta, 5);
       tc_fence_before();
       mbar_arrive(bar_tempty(ab));
       ++sg;
@@ -678,6 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // no CTA leaves while a peer may still multicast into it or arrive on it
+  if (g.cs > 1) cluster_sync();
+  if (threadIdx.x == 0) PDS_GEMM_TRACE_HOOK(cta, 6);
   if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
@@ -706,11 +765,15 @@ EncodeTiledFn encode_fn() {
 struct TmapKey {
   const void* p;
   uint64_t inner, outer;
-  bool operator==(const TmapKey& o) const { return p == o.p && inner == o.inner && outer == o.outer; }
+  uint32_t box_rows;
+  bool operator==(const TmapKey& o) const {
+    return p == o.p && inner == o.inner && outer == o.outer && box_rows == o.box_rows;
+  }
 };
 struct TmapKeyHash {
   size_t operator()(const TmapKey& k) const {
-    return std::hash<const void*>()(k.p) ^ (k.inner * 0x9E3779B97F4A7C15ull) ^ (k.outer << 20);
+    return std::hash<const void*>()(k.p) ^ (k.inner * 0x9E3779B97F4A7C15ull) ^ (k.outer << 20) ^
+           (static_cast<size_t>(k.box_rows) << 44);
   }
 };
 struct TmapCache {
@@ -723,10 +786,11 @@ void tmap_cache_destroy(TmapCache* c) { delete c; }
 
 namespace {
 
-// bf16 matrix [outer rows, inner columns], box of 64 columns x 128 rows, 128-byte swizzle.
+// bf16 matrix [outer rows, inner columns], box of 64 columns x box_rows rows,
+// 128-byte swizzle.
 pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner, uint64_t outer,
-                   std::string* err) {
-  TmapKey key{p, inner, outer};
+                   std::string* err, uint32_t box_rows = 128) {
+  TmapKey key{p, inner, outer, box_rows};
   if (c.maps) {
     std::lock_guard<std::mutex> g(c.maps->mu);
     auto it = c.maps->maps.find(key);
@@ -742,7 +806,7 @@ pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner
   }
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), 128};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
   const cuuint32_t es[2] = {1, 1};
   CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, box,
                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -758,7 +822,12 @@ pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner
   return PDS_OK;
 }
 
-void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K,
+// Rows of a weight box: the slice one CTA of a cluster loads.
+uint32_t weight_box_rows(const GemmArgs& g, int bn) {
+  return g.cs > 1 ? static_cast<uint32_t>(bn / g.cs) : 128u;
+}
+
+void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, int bn,
                    int max_grid = kGemmMaxGrid) {
   g.M = M;
   g.K = K;
@@ -772,6 +841,18 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K,
   g.mgs = g.tiles_m / gs;
   g.units = g.mgs * g.tiles_n;
   g.total = g.units * g.kb;
+  // Cluster size: the largest of 4, 2 dividing the group whose weight slice is
+  // at least 64 rows.  PDS_GEMM_CLUSTER=1 turns multicast off (a tuning knob).
+  static const int env_cs = [] {
+    const char* v = std::getenv("PDS_GEMM_CLUSTER");
+    return v ? std::max(1, std::atoi(v)) : 4;
+  }();
+  g.cs = 1;
+  for (int cs = 4; cs >= 2; cs /= 2)
+    if (cs <= env_cs && gs % cs == 0 && bn / cs >= 64) {
+      g.cs = cs;
+      break;
+    }
   // PDS_GEMM_CTAS caps the CTAs of every GEMM (a tuning knob; default: one per SM).
   static const int env_cap = [] {
     const char* v = std::getenv("PDS_GEMM_CTAS");
@@ -829,15 +910,46 @@ pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t 
   g.counters = reinterpret_cast<uint32_t*>(c.ws + part_bytes);
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(g.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cf::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (g.cs > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = g.cs;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    // never more clusters than fit on the GPU at once (one CTA per SM)
+    static std::mutex mu;
+    static int max_clusters[5] = {0, 0, 0, 0, 0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!max_clusters[g.cs]) {
+      cfg.gridDim = dim3(g.cs);
+      cfg.attrs = attr;
+      cfg.numAttrs = na;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, EPI>, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = 1;
+      }
+      max_clusters[g.cs] = n;
+    }
+    const int cap_groups = std::max(1, max_clusters[g.cs] * g.cs / g.gs);
+    if (g.groups > cap_groups) {
+      g.groups = cap_groups;
+      g.grid = g.groups * g.gs;
+    }
+  }
+  if (c.pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.gridDim = dim3(g.grid);
   cfg.attrs = attr;
-  cfg.numAttrs = c.pdl ? 1 : 0;
+  cfg.numAttrs = na;
   cudaError_t ce = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, EPI>, maps, g);
   if (ce != cudaSuccess) {
     *err = std::string("gemm launch: ") + cudaGetErrorString(ce);
@@ -856,67 +968,59 @@ size_t tc_gemm_scratch_bytes(int M, int max_tiles_n) {
 
 pds_status tc_gemm_plain(TcContext& c, const uint16_t* A, const uint16_t* W, float* Cout, int M,
                          int N, int K, cudaStream_t st, std::string* err) {
-  GemmMaps maps;
-  pds_status rc;
-  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[0], W, K, N, err)) != PDS_OK) return rc;
-  maps.b[1] = maps.b[0];
-  maps.b[2] = maps.b[0];
+  const int bn = N % 256 == 0 ? 256 : 128;
   GemmArgs g{};
   g.wrows0 = N;
   g.wrows1 = 0;
   g.c_out = Cout;
   g.ldc = N;
-  if (N % 256 == 0) {
-    make_schedule(g, c, M, N / 256, K);
-    return launch<256, kEpiPlain>(c, maps, g, st, err);
-  }
-  make_schedule(g, c, M, N / 128, K);
-  return launch<128, kEpiPlain>(c, maps, g, st, err);
+  make_schedule(g, c, M, N / bn, K, bn);
+  GemmMaps maps;
+  pds_status rc;
+  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, bn))) != PDS_OK) return rc;
+  maps.b[1] = maps.b[0];
+  maps.b[2] = maps.b[0];
+  return bn == 256 ? launch<256, kEpiPlain>(c, maps, g, st, err)
+                   : launch<128, kEpiPlain>(c, maps, g, st, err);
 }
 
 pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int M, int N, int K,
                          const ResidEpilogue& e, cudaStream_t st, std::string* err) {
-  GemmMaps maps;
-  pds_status rc;
-  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[0], W, K, N, err)) != PDS_OK) return rc;
-  maps.b[1] = maps.b[0];
-  maps.b[2] = maps.b[0];
+  const int bn = N % 256 == 0 ? 256 : 128;
   GemmArgs g{};
   g.wrows0 = N;
   g.resid = e;
   g.resid_n = N;
-  if (N % 256 == 0) {
-    make_schedule(g, c, M, N / 256, K);
-    return launch<256, kEpiResid>(c, maps, g, st, err);
-  }
-  make_schedule(g, c, M, N / 128, K);
-  return launch<128, kEpiResid>(c, maps, g, st, err);
+  make_schedule(g, c, M, N / bn, K, bn);
+  GemmMaps maps;
+  pds_status rc;
+  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, bn))) != PDS_OK) return rc;
+  maps.b[1] = maps.b[0];
+  maps.b[2] = maps.b[0];
+  return bn == 256 ? launch<256, kEpiResid>(c, maps, g, st, err)
+                   : launch<128, kEpiResid>(c, maps, g, st, err);
 }
 
 pds_status tc_gemm_swiglu(TcContext& c, const uint16_t* A, const WeightRows& W, int M, int K,
                           const SwigluEpilogue& e, cudaStream_t st, std::string* err) {
-  GemmMaps maps;
-  pds_status rc;
-  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[0], W.w[0], K, W.rows[0], err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[1], W.w[1], K, W.rows[1], err)) != PDS_OK) return rc;
-  maps.b[2] = maps.b[0];
   GemmArgs g{};
   g.pair_mode = 1;
   g.swiglu = e;
-  make_schedule(g, c, M, e.ffn / 128, K);
+  make_schedule(g, c, M, e.ffn / 128, K, 256);
+  GemmMaps maps;
+  pds_status rc;
+  const uint32_t br = weight_box_rows(g, 256);
+  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[0], W.w[0], K, W.rows[0], err, br)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[1], W.w[1], K, W.rows[1], err, br)) != PDS_OK) return rc;
+  maps.b[2] = maps.b[0];
   return launch<256, kEpiSwiglu>(c, maps, g, st, err);
 }
 
 pds_status tc_gemm_qkv(TcContext& c, const uint16_t* A, const WeightRows& W, int M, int K,
                        const QkvEpilogue& e, cudaStream_t st, std::string* err) {
-  GemmMaps maps;
-  pds_status rc;
-  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  for (int i = 0; i < 3; ++i)
-    if ((rc = get_map(c, &maps.b[i], W.w[i], K, W.rows[i], err)) != PDS_OK) return rc;
   GemmArgs g{};
   g.wrows0 = W.rows[0];
   g.wrows1 = W.rows[1];
@@ -924,7 +1028,13 @@ pds_status tc_gemm_qkv(TcContext& c, const uint16_t* A, const WeightRows& W, int
   const int N = W.rows[0] + W.rows[1] + W.rows[2];
   // 256-column tiles always (each 128-column half holds whole heads); a
   // last half past N reads zero rows and is skipped by the epilogue.
-  make_schedule(g, c, M, (N + 255) / 256, K);
+  make_schedule(g, c, M, (N + 255) / 256, K, 256);
+  GemmMaps maps;
+  pds_status rc;
+  const uint32_t br = weight_box_rows(g, 256);
+  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
+  for (int i = 0; i < 3; ++i)
+    if ((rc = get_map(c, &maps.b[i], W.w[i], K, W.rows[i], err, br)) != PDS_OK) return rc;
   return launch<256, kEpiQkv>(c, maps, g, st, err);
 }
 
@@ -1007,16 +1117,18 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   }
   TcContext c{};
   c.num_sms = num_sms;
-  GemmMaps maps;
-  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[0], W, K, N, err)) != PDS_OK) return rc;
-  maps.b[1] = maps.b[0];
-  maps.b[2] = maps.b[0];
   GemmArgs g{};
   g.wrows0 = N;
   g.c_out = Cout;
   g.ldc = N;
-  make_schedule(g, c, M, N / kNoAllocBN, K, grid_cap);
+  make_schedule(g, c, M, N / kNoAllocBN, K, kNoAllocBN, grid_cap);
+  g.cs = 1;  // a plain launch, without clusters
+  GemmMaps maps;
+  if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, kNoAllocBN))) != PDS_OK)
+    return rc;
+  maps.b[1] = maps.b[0];
+  maps.b[2] = maps.b[0];
   g.status = status;
   g.partials = partials;
   g.counters = counters;
