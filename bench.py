@@ -240,9 +240,9 @@ def main():
     out_dev = torch.empty_like(x_dev)
     B, s = dims.batch, dims.start_pos
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
+    from dense_decoder_layer_gb300 import replicas
+
+    barrier = replicas.barrier
 
     def step():
         st.prefill_device(x_dev, s, out_dev)
@@ -265,13 +265,8 @@ def main():
     barrier()
     clock_info = clocks.stop()
     st.sync()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, value = replicas.aggregate(e0.elapsed_time(e1), B * args.steps)
     ms_per_step = ms / args.steps
-    value = world * B * args.steps / (ms / 1e3)
 
     # end to end through the host-I/O entry point (pinned host buffers)
     h_in = torch.from_numpy(hidden).pin_memory()
@@ -288,12 +283,7 @@ def main():
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     barrier()
-    e2e_ms = max(e0.elapsed_time(e1), wall * 1e3)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * B * args.steps / (e2e_ms / 1e3)
+    e2e_ms, e2e_value = replicas.aggregate(max(e0.elapsed_time(e1), wall * 1e3), B * args.steps)
 
     # per-kernel durations: same steps with events around every kernel
     pds.pds_plan_set_timing(st.plan, True)

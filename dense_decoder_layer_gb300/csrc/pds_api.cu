@@ -169,6 +169,10 @@ static pds_status check_call(pds_plan* plan, const pds_layer* layers, uint16_t* 
         return fail(PDS_EINVAL, "layer " + std::to_string(l) + ": pointer not 16-byte aligned");
     }
   }
+  // Fault injection for the callers' failure handling: the call is admitted,
+  // then fails as a launch would, before any device work.
+  if (env_flag("PDS_FAULT_AFTER_ADMIT"))
+    return fail(PDS_ELAUNCH, "injected failure after admission (PDS_FAULT_AFTER_ADMIT)");
   return PDS_OK;
 }
 
@@ -220,6 +224,15 @@ pds_status pds_plan_sync(pds_plan* plan, void* stream) {
   pds_status st = pds::plan_sync(*plan, static_cast<cudaStream_t>(stream), &err);
   if (st != PDS_OK) return fail(st, err);
   return PDS_OK;
+}
+
+pds_status pds_selftest_stuck_wait(uint32_t limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 10000000u)
+    return fail(PDS_EINVAL, "pds_selftest_stuck_wait: limit_us must be in (0, 10 s]");
+  std::string err;
+  pds_status st = pds::run_stuck_wait(limit_us, static_cast<cudaStream_t>(stream), &err);
+  t_last_error = err;  // an ETIMEOUT here is the expected outcome, not a failure to report
+  return st;
 }
 
 pds_status pds_plan_set_timing(pds_plan* plan, int32_t enable) {

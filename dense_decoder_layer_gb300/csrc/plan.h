@@ -77,6 +77,7 @@ void plan_release_device(Plan& p);
 
 pds_status run_gemm_plain(const uint16_t* A, const uint16_t* W, float* C, int M, int N, int K,
                           char* ws, size_t ws_bytes, cudaStream_t st, std::string* err);
+pds_status run_stuck_wait(uint32_t limit_us, cudaStream_t st, std::string* err);
 pds_status run_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
                          int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
                          std::string* err);

@@ -82,6 +82,7 @@ def load() -> ctypes.CDLL:
         "pds_gemm_bf16_noalloc": (st, [vp, vp, vp, i32, i32, i32, vp]),
         "pds_attention": (st, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "pds_plan_set_timing": (st, [vp, i32]),
+        "pds_selftest_stuck_wait": (st, [ctypes.c_uint32, vp]),
         "pds_plan_kernel_times": (st, [vp, vp, ctypes.POINTER(pds_kernel_times), i32]),
     }
     for name, (res, args) in sig.items():
@@ -189,3 +190,8 @@ def pds_plan_kernel_times(plan, stream, reset: bool = False) -> dict:
     kt = pds_kernel_times()
     check(load().pds_plan_kernel_times(plan, stream, ctypes.byref(kt), 1 if reset else 0))
     return {k: (kt.launches[i], kt.total_ms[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def pds_selftest_stuck_wait(limit_us: int, stream) -> int:
+    """Status of the bounded-wait self test (PDS_ETIMEOUT is the expected answer)."""
+    return load().pds_selftest_stuck_wait(limit_us, stream)

@@ -188,6 +188,16 @@ typedef struct pds_kernel_times {
   double total_ms[PDS_KERNEL_KINDS];
 } pds_kernel_times;
 
+/*
+ * Failure-detection self test (no counterpart on the pages).  Runs a
+ * one-CTA kernel that waits on an mbarrier nothing ever arrives on, through
+ * the same bounded wait every tensor-core kernel of the library uses, with
+ * a limit of limit_us microseconds.  Returns PDS_ETIMEOUT when the wait gave
+ * up, set the timeout bit and let the kernel exit (the expected outcome),
+ * PDS_OK if the wait somehow completed.  Synchronizes the stream.
+ */
+pds_status pds_selftest_stuck_wait(uint32_t limit_us, void* stream);
+
 pds_status pds_plan_set_timing(pds_plan* plan, int32_t enable);
 pds_status pds_plan_kernel_times(pds_plan* plan, void* stream, pds_kernel_times* out,
                                  int32_t reset);
