@@ -63,6 +63,37 @@ def flops(dims):
     return per, dims.n_layers * sum(per.values())
 
 
+KERNEL_SOURCES = ("gemm_tc.cu", "sm100.cuh", "attn.cu", "tc.h", "kernels.h", "common.cuh")
+
+
+def kernel_source_sha():
+    """sha256 prefix of the kernel sources, to tell whether a profile is current."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dense_decoder_layer_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kind, workload):
+    """DRAM bytes per launch of one kernel from the committed ncu summary, or
+    None when that summary was taken on other kernel sources or workload."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        with open(path) as f:
+            kv = dict(line.split(None, 1) for line in f
+                      if line.strip() and not line.startswith("#"))
+    except (OSError, ValueError):
+        return None
+    if kv.get("source_sha", "").strip() != kernel_source_sha():
+        return None
+    if kv.get("workload", "").strip() != workload or kind not in kv:
+        return None
+    return int(kv[kind])
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -314,7 +345,8 @@ def main():
     roofline = {
         "kernel": f"gemm_{dom}", "bound": "tensor",
         "achieved": kernels[dom]["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
-        "frac": kernels[dom]["tflops"] / peak_tf, "traffic": None,
+        "frac": kernels[dom]["tflops"] / peak_tf,
+        "traffic": measured_traffic(dom, args.workload), "traffic_unit": "bytes per launch",
         "peak_source": f"{peak_src} bf16_tflops_sustained",
         "gemm_frac": gemm_flop / (gemm_ms / 1e3) / 1e12 / peak_tf,
         "end_to_end_frac": total_flop / (ms_per_step / 1e3) / 1e12 / peak_tf,
