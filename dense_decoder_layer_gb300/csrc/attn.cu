@@ -3,9 +3,10 @@
 // prefix_k / prefix_v are the cache's first start_pos rows; attn_scale =
 // 1/sqrt(head_dim); no softcap, no window).
 //
-// Flash-style: one CTA per (64 query rows, query head), 4 warps of 16 rows.
-// K/V tiles of 64 keys are staged in shared memory (double-buffered async
-// copies, XOR-swizzled 16-byte chunks so ldmatrix is conflict-free);
+// Flash-style: one CTA per (64 query rows, query head), two halves of 4
+// warps (16 rows each) that split the key tiles between them.  K/V tiles of
+// 64 keys are staged in shared memory (double-buffered async copies per
+// half, XOR-swizzled 16-byte chunks so ldmatrix is conflict-free);
 // S = Q.K^T and O += P.V run on the tensor cores (bf16 in, fp32 out); the
 // softmax is online, in base 2, with the running max and sum per row kept
 // by the 4 threads that own the row.  Key tiles past the CTA's last
@@ -38,6 +39,9 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -66,36 +70,49 @@ __device__ __forceinline__ int swz(int row, int chunk) {
   return row * HD + ((chunk ^ (row & 7)) << 3);
 }
 
+// The two halves of a CTA (warps 0-3 and 4-7) take alternate key tiles of
+// the same 64 query rows, each with its own double-buffered K/V tiles and
+// its own running max, sum and output; at the end the second half hands its
+// state to the first through shared memory and the first merges the two.
 template <int HD>
-__global__ void __launch_bounds__(128) flash_attn_kernel(const uint16_t* __restrict__ q,
+__global__ void __launch_bounds__(256) flash_attn_kernel(const uint16_t* __restrict__ q,
                                                          const uint16_t* __restrict__ k,
                                                          const uint16_t* __restrict__ v,
                                                          uint16_t* __restrict__ o, int B, int s,
                                                          int H, int Hkv, float scale_log2) {
   constexpr int CH = HD / 8;  // 16-byte chunks per row
   extern __shared__ __align__(128) uint16_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kh = warp >> 2;   // which half: key tiles kh, kh + 2, ...
+  const int wq = warp & 3;    // which 16 query rows
+  const int htid = tid & 127;
   uint16_t* sQ = smem;
-  uint16_t* sK = sQ + kBM * HD;
+  uint16_t* sK = sQ + kBM * HD + kh * (4 * kBN * HD);  // this half's 2 K then 2 V tiles
   uint16_t* sV = sK + 2 * kBN * HD;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
-  const int h = blockIdx.y, g = h / (H / Hkv);
+  const int qt = gridDim.y - 1 - blockIdx.y;  // longest row tiles first, over all heads
+  const int h = blockIdx.x, g = h / (H / Hkv);
   const int b0 = qt * kBM;
   const int T = s + B;
   const int last_row = min(b0 + kBM, B) - 1;
   const int kv_end = s + last_row + 1;
   const int nkt = (kv_end + kBN - 1) / kBN;
+  const int nmine = nkt > kh ? (nkt - kh + 1) / 2 : 0;
 
-  for (int i = tid; i < kBM * CH; i += 128) {
+  // q, k and v are the previous kernel's output
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  for (int i = tid; i < kBM * CH; i += 256) {
     const int r = i / CH, c = i % CH, b = b0 + r;
     cp_async16(smem_addr(sQ + swz<HD>(r, c)),
                q + (static_cast<size_t>(min(b, B - 1)) * H + h) * HD + c * 8, b < B ? 16 : 0);
   }
+  cp_async_commit();
   auto load_kv = [&](int kt, int buf) {
     uint16_t* dk = sK + buf * kBN * HD;
     uint16_t* dv = sV + buf * kBN * HD;
-    for (int i = tid; i < kBN * CH; i += 128) {
+    for (int i = htid; i < kBN * CH; i += 128) {
       const int r = i / CH, c = i % CH, j = kt * kBN + r;
       const size_t off = (static_cast<size_t>(min(j, T - 1)) * Hkv + g) * HD + c * 8;
       const int n = j < T ? 16 : 0;
@@ -103,31 +120,32 @@ __global__ void __launch_bounds__(128) flash_attn_kernel(const uint16_t* __restr
       cp_async16(smem_addr(dv + swz<HD>(r, c)), v + off, n);
     }
   };
-  load_kv(0, 0);
+  if (nmine > 0) load_kv(kh, 0);
   cp_async_commit();
+  cp_async_wait<1>();  // this thread's part of Q
+  __syncthreads();     // everyone's
 
   uint32_t qf[HD / 16][4];
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const int row = wq * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    ldsm_x4(qf[kk], smem_addr(sQ + swz<HD>(row, kk * 2 + (lane >> 4))));
+  }
   float oacc[HD / 8][4];
 #pragma unroll
   for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  const int r_lo = warp * 16 + (lane >> 2);
+  const int r_lo = wq * 16 + (lane >> 2);
   const int pos0 = s + b0 + r_lo, pos1 = pos0 + 8;
-  const int warp_min_pos = s + b0 + warp * 16;
+  const int warp_min_pos = s + b0 + wq * 16;
 
-  for (int kt = 0; kt < nkt; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < nkt) load_kv(kt + 1, buf ^ 1);
+  for (int it = 0; it < nmine; ++it) {
+    const int kt = kh + 2 * it;
+    const int buf = it & 1;
+    if (it + 1 < nmine) load_kv(kt + 2, buf ^ 1);
     cp_async_commit();
     cp_async_wait<1>();
-    __syncthreads();
-    if (kt == 0) {
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        ldsm_x4(qf[kk], smem_addr(sQ + swz<HD>(row, kk * 2 + (lane >> 4))));
-      }
-    }
+    named_barrier(1 + kh, 128);
     const uint16_t* tK = sK + buf * kBN * HD;
     const uint16_t* tV = sV + buf * kBN * HD;
 
@@ -204,10 +222,34 @@ __global__ void __launch_bounds__(128) flash_attn_kernel(const uint16_t* __restr
         mma_bf16(oacc[nb + 1], pf[kk], b[2], b[3]);
       }
     }
-    __syncthreads();
+    named_barrier(1 + kh, 128);  // the tile is consumed before its buffer is refilled
   }
 
-  float l0 = l_run[0], l1 = l_run[1];
+  // Merge: the second half's state through shared memory (the K/V tiles'
+  // space, free now), in the fragment layout, one word per lane.
+  cp_async_wait<0>();
+  __syncthreads();
+  constexpr int kWords = HD / 2 + 4;  // oacc, then m, l per fragment row
+  float* xch = reinterpret_cast<float*>(smem + kBM * HD) + wq * (kWords * 32);
+  if (kh == 1) {
+#pragma unroll
+    for (int nb = 0; nb < HD / 8; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) xch[(nb * 4 + e) * 32 + lane] = oacc[nb][e];
+    xch[(HD / 2 + 0) * 32 + lane] = m_run[0];
+    xch[(HD / 2 + 1) * 32 + lane] = m_run[1];
+    xch[(HD / 2 + 2) * 32 + lane] = l_run[0];
+    xch[(HD / 2 + 3) * 32 + lane] = l_run[1];
+  }
+  __syncthreads();
+  if (kh == 1) return;
+  const float m1a = xch[(HD / 2 + 0) * 32 + lane], m1b = xch[(HD / 2 + 1) * 32 + lane];
+  const float m0 = fmaxf(m_run[0], m1a), m1 = fmaxf(m_run[1], m1b);
+  // the first half always sees key 0, so m0 and m1 are finite
+  const float a00 = exp2f(m_run[0] - m0), a10 = exp2f(m1a - m0);
+  const float a01 = exp2f(m_run[1] - m1), a11 = exp2f(m1b - m1);
+  float l0 = l_run[0] * a00 + xch[(HD / 2 + 2) * 32 + lane] * a10;
+  float l1 = l_run[1] * a01 + xch[(HD / 2 + 3) * 32 + lane] * a11;
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -216,27 +258,42 @@ __global__ void __launch_bounds__(128) flash_attn_kernel(const uint16_t* __restr
   const int row0 = b0 + r_lo, row1 = row0 + 8;
 #pragma unroll
   for (int nb = 0; nb < HD / 8; ++nb) {
+    const float o0 = oacc[nb][0] * a00 + xch[(nb * 4 + 0) * 32 + lane] * a10;
+    const float o1 = oacc[nb][1] * a00 + xch[(nb * 4 + 1) * 32 + lane] * a10;
+    const float o2 = oacc[nb][2] * a01 + xch[(nb * 4 + 2) * 32 + lane] * a11;
+    const float o3 = oacc[nb][3] * a01 + xch[(nb * 4 + 3) * 32 + lane] * a11;
     const int col = h * HD + nb * 8 + 2 * (lane & 3);
     if (row0 < B)
       *reinterpret_cast<uint32_t*>(o + static_cast<size_t>(row0) * H * HD + col) =
-          pack_bf16x2(oacc[nb][0] * inv0, oacc[nb][1] * inv0);
+          pack_bf16x2(o0 * inv0, o1 * inv0);
     if (row1 < B)
       *reinterpret_cast<uint32_t*>(o + static_cast<size_t>(row1) * H * HD + col) =
-          pack_bf16x2(oacc[nb][2] * inv1, oacc[nb][3] * inv1);
+          pack_bf16x2(o2 * inv1, o3 * inv1);
   }
 }
 
 template <int HD>
 cudaError_t launch_flash(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
-                         int B, int s, int H, int Hkv, cudaStream_t st) {
-  constexpr size_t smem = static_cast<size_t>(kBM + 4 * kBN) * HD * sizeof(uint16_t);
+                         int B, int s, int H, int Hkv, bool pdl, cudaStream_t st) {
+  constexpr size_t smem = static_cast<size_t>(kBM + 8 * kBN) * HD * sizeof(uint16_t);
+  static_assert((HD / 2 + 4) * 32 * 4 * 4 <= 8 * kBN * HD * 2, "merge area");
   static cudaError_t attr = cudaFuncSetAttribute(
       flash_attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (attr != cudaSuccess) return attr;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  dim3 grid((B + kBM - 1) / kBM, H);
-  flash_attn_kernel<HD><<<grid, 128, smem, st>>>(q, k, v, o, B, s, H, Hkv, scale_log2);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(H, (B + kBM - 1) / kBM);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute a[1];
+  if (pdl) {
+    a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, flash_attn_kernel<HD>, q, k, v, o, B, s, H, Hkv, scale_log2);
 }
 
 }  // namespace
@@ -244,9 +301,8 @@ cudaError_t launch_flash(const uint16_t* q, const uint16_t* k, const uint16_t* v
 pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
                         std::string* err) {
-  (void)c;
-  cudaError_t ce = hd == 128 ? launch_flash<128>(q, k, v, o, B, start_pos, H, Hkv, st)
-                             : launch_flash<64>(q, k, v, o, B, start_pos, H, Hkv, st);
+  cudaError_t ce = hd == 128 ? launch_flash<128>(q, k, v, o, B, start_pos, H, Hkv, c.pdl, st)
+                             : launch_flash<64>(q, k, v, o, B, start_pos, H, Hkv, c.pdl, st);
   if (ce != cudaSuccess) {
     *err = std::string("attention launch: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;

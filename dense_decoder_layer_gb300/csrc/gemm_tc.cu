@@ -38,6 +38,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -64,6 +65,9 @@ constexpr int kMinItersPerCta = 4;
 struct GemmMaps {
   CUtensorMap a;
   CUtensorMap b[3];
+  // residual epilogue through shared memory: [0] residual load (float32,
+  // 32 x 128 boxes), [1] h store (float32, 32 x 32), [2] a store (bf16, 64 x 32)
+  CUtensorMap e[3];
 };
 
 struct GemmArgs {
@@ -98,11 +102,23 @@ struct Cfg {
   static constexpr uint32_t kBBytes = BN * BK * 2;
   static constexpr uint32_t kStage = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
-  static constexpr int kBars = 2 * kStages + 5;
-  static constexpr uint32_t kMiscBytes = 1024;                  // barriers + misc words
+  static constexpr int kBars = 2 * kStages + 5 + 4;
+  // The last tile's residual epilogue reuses the drained stages: 16 KB boxes,
+  // BN/32 float32 residual boxes (32 columns x 128 rows) then BN/64 bf16 boxes
+  // of the next GEMM's operand (64 columns x 128 rows).
+  static constexpr int kBoxesPerStage = static_cast<int>(kStage / 16384);
+  static constexpr int kResBoxes = BN / 32;
+  static constexpr int kResStages = (kResBoxes + kBoxesPerStage - 1) / kBoxesPerStage;
+  // then 4 boxes of other CTAs' partial tiles (2 buffers per column half)
+  static constexpr int kPartBoxes = 4;
+  static_assert((kResBoxes + kPartBoxes + kBoxesPerStage - 1) / kBoxesPerStage <= kStages,
+                "epilogue boxes fit in the stages");
+  static_assert(BN * 4 <= 1024, "gain area");
+  static_assert(kResStages <= 4, "residual barriers");
+  static constexpr uint32_t kMiscBytes = 2048;  // barriers + misc words; the gain from 1024 on
   static constexpr uint32_t kStageBytes = 8 * 32 * 128;         // epilogue staging, 4 KB a warp
   static constexpr size_t kSmem = 1024 + kStages * kStage + kMiscBytes + kStageBytes;
-  static_assert(kBars * 8 + 16 <= kMiscBytes, "barrier area");
+  static_assert(kBars * 8 + 16 <= 1024, "barrier area");
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
@@ -252,6 +268,13 @@ __device__ __forceinline__ void acc_pair(const GemmArgs& g, uint32_t taddr, cons
   acc_sub<BN>(g, taddr, fx, jb, hb, row, vb);
 }
 
+// x^2 + y^2 + z^2 + w^2 with a fixed rounding order (no contraction), so
+// that every epilogue path gives the same statistics bit for bit.
+__device__ __forceinline__ float sumsq4(float4 h) {
+  return __fadd_rn(__fadd_rn(__fmul_rn(h.x, h.x), __fmul_rn(h.y, h.y)),
+                   __fadd_rn(__fmul_rn(h.z, h.z), __fmul_rn(h.w, h.w)));
+}
+
 struct Stage {
   float4* base;
   __device__ __forceinline__ float4& at(int row, int q) const { return base[row * 8 + (q ^ (row & 7))]; }
@@ -380,7 +403,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
                   reinterpret_cast<uint2*>(e.a_out + off),
                   make_uint2(pack_bf16x2(h4.x * g4.x, h4.y * g4.y), pack_bf16x2(h4.z * g4.z, h4.w * g4.w)),
                   pol_keep);
-            float s = h4.x * h4.x + h4.y * h4.y + h4.z * h4.z + h4.w * h4.w;
+            float s = sumsq4(h4);
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             s += __shfl_xor_sync(0xffffffffu, s, 4);
@@ -482,6 +505,190 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
   }
 }
 
+// Shared-memory address of epilogue box b of a CTA's last tile: the boxes
+// fill the stages in the order the ring frees them after the CTA's n_it
+// k-blocks, kBoxesPerStage to a stage.
+template <int BN>
+__device__ __forceinline__ uint32_t epi_box(uint32_t sbase, int n_it, int b) {
+  using C = Cfg<BN>;
+  const int s = (n_it + b / C::kBoxesPerStage) % C::kStages;
+  return sbase + static_cast<uint32_t>(s) * C::kStage +
+         static_cast<uint32_t>(b % C::kBoxesPerStage) * 16384u;
+}
+
+// Finishes a split tile that this CTA completes as its last tile, in TMEM:
+// for each 32-column chunk this thread's epilogue reads, the contributors'
+// accumulators are summed in k order from zero (its own TMEM value in its
+// place), as the register path does, and written back to TMEM.  Every
+// thread copies only its own row of the other contributors' partial tiles
+// (cp.async, one copy ahead, two buffers per column half in the drained
+// stages from box `box0` on), so no thread waits for another.
+template <int BN, int EPI>
+__device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup& fx,
+                                                  uint32_t taddr, int nt, int row, int ch,
+                                                  uint32_t sbase, int n_it, int box0) {
+  using namespace sm100;
+  constexpr int kOwned = owned_chunks<BN, EPI>();
+  const int nother = fx.gl - fx.gf;  // contributors other than this CTA's group
+  // the t-th other contributor in k order, and copy k: (owned chunk, contributor)
+  auto contributor = [&](int t) { return fx.gf + t + (fx.gf + t >= fx.me ? 1 : 0); };
+  auto issue = [&](int k) {
+    const int i = k / nother, t = k - (k / nother) * nother;
+    const int j = owned_chunk<BN, EPI>(ch, i);
+    const uint32_t dst = epi_box<BN>(sbase, n_it, box0 + ch * 2 + (k & 1)) +
+                         static_cast<uint32_t>(row) * 16u;
+    const float4* src = partial_slot(g, contributor(t), fx.r, fx.unit, BN) +
+                        static_cast<size_t>(j * 8) * BM + row;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + q * BM * 16u),
+                   "l"(src + q * BM)
+                   : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  const int nloads = kOwned * nother;
+  issue(0);
+  int k = 0;
+#pragma unroll 1
+  for (int i = 0; i < kOwned; ++i) {
+    const int j = owned_chunk<BN, EPI>(ch, i);
+    const bool exists = chunk_exists<BN, EPI>(g, nt, j);
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) v[q] = 0.f;
+#pragma unroll 1
+    for (int c = fx.gf; c <= fx.gl; ++c) {
+      if (c == fx.me) {
+        if (exists) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float own[16];
+            tmem_load16(taddr + j * 32 + h * 16, own);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[h * 16 + q] += own[q];
+          }
+        }
+        continue;
+      }
+      if (k + 1 < nloads) {
+        issue(k + 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+      }
+      const uint32_t pb = epi_box<BN>(sbase, n_it, box0 + ch * 2 + (k & 1)) +
+                          static_cast<uint32_t>(row) * 16u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 p = ld_shared_f4(pb + q * BM * 16u);
+        v[4 * q] += p.x;
+        v[4 * q + 1] += p.y;
+        v[4 * q + 2] += p.z;
+        v[4 * q + 3] += p.w;
+      }
+      ++k;
+    }
+    if (exists) tmem_store32(taddr + j * 32, v);
+  }
+}
+
+// Residual epilogue of a CTA's last tile, through shared memory.  The
+// producer has loaded the residual tile into the drained stages (one barrier
+// per stage).  Each thread adds its row's accumulator (TMEM; a split tile
+// has been finished there first) to the residual in place (h), writes
+// bf16(h * gain) to its warp's staging area and sums h^2 per 64 columns;
+// each warp then stores its 32 rows of each box with TMA.  No global load
+// or store of a tile element goes through registers.  Returns false if a
+// wait gave up.
+template <int BN>
+__device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const GemmMaps& maps,
+                                                    uint32_t taddr, int mt, int nt, int row,
+                                                    int ch, int lane, uint32_t sbase, int n_it,
+                                                    uint32_t bar_res0, volatile int* abort_flag,
+                                                    const Stage& st, float* gain_sm) {
+  using namespace sm100;
+  using C = Cfg<BN>;
+  constexpr int EPI = kEpiResid;  // for the trace hook
+  (void)EPI;
+  constexpr int kChunks = BN / 64;  // 32-column chunks of this thread's half
+  const ResidEpilogue& e = g.resid;
+  const int lane_grp = row >> 5;
+  const int m = mt * BM + row;
+  const int m0w = mt * BM + lane_grp * 32;
+  const bool warp_live = m0w < g.M;
+  const uint64_t pol_keep = policy_evict_last();
+  const uint32_t sw = static_cast<uint32_t>(row & 7);
+  const uint32_t a_stage = smem_u32(st.base);  // this warp's 32 rows x 64 bf16 of the operand
+  // The gain of this half's columns, once, by the half's first warp.
+  if (e.gain) {
+    if (lane_grp == 0 && lane < BN / 8)
+      reinterpret_cast<float4*>(gain_sm)[ch * (BN / 8) + lane] =
+          __ldg(reinterpret_cast<const float4*>(e.gain + nt * BN + ch * (BN / 2)) + lane);
+    named_bar_sync(2 + ch, 128);
+  }
+  const float4* gs = reinterpret_cast<const float4*>(gain_sm) + ch * (BN / 8);
+  float ss = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < kChunks; ++c) {
+    const int j = ch * kChunks + c;  // 32-column chunk = residual box j
+    const int n0 = nt * BN + j * 32;
+    if (!mbar_wait(bar_res0 + 8u * (j / C::kBoxesPerStage), 0, abort_flag, g.status)) return false;
+    if (c == 0 && row == 0 && ch == 0) PDS_GEMM_TRACE_HOOK(blockIdx.x, 7);
+    float v[32];
+    tmem_load32(taddr + j * 32, v);
+    const uint32_t rrow = epi_box<BN>(sbase, n_it, j) + static_cast<uint32_t>(row) * 128u;
+    if (e.gain && (c & 1) == 0 && c > 0) {
+      // the previous pair's operand store has read the staging area
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+    }
+    float t[8];
+#pragma unroll
+    for (int q2 = 0; q2 < 4; ++q2) {
+      float4 h[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = 2 * q2 + u;
+        const uint32_t addr = rrow + ((static_cast<uint32_t>(q) ^ sw) << 4);
+        const float4 r = ld_shared_f4(addr);
+        h[u] = make_float4(r.x + v[4 * q], r.y + v[4 * q + 1], r.z + v[4 * q + 2],
+                           r.w + v[4 * q + 3]);
+        st_shared_f4(addr, h[u]);
+        t[q] = sumsq4(h[u]);
+      }
+      if (e.gain) {
+        const float4 ga = gs[c * 8 + 2 * q2], gb = gs[c * 8 + 2 * q2 + 1];
+        const uint32_t ac = static_cast<uint32_t>((j & 1) * 4 + q2);
+        st_shared_u4(a_stage + static_cast<uint32_t>(lane) * 128u + ((ac ^ sw) << 4),
+                     pack_bf16x2(h[0].x * ga.x, h[0].y * ga.y),
+                     pack_bf16x2(h[0].z * ga.z, h[0].w * ga.w),
+                     pack_bf16x2(h[1].x * gb.x, h[1].y * gb.y),
+                     pack_bf16x2(h[1].z * gb.z, h[1].w * gb.w));
+      }
+    }
+    // the 32 columns' sum in the register path's shuffle-tree order
+    ss += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && warp_live)
+      tma_store_2d(&maps.e[1], epi_box<BN>(sbase, n_it, j) + lane_grp * 4096u, n0, m0w, pol_keep);
+    if (e.gain && (j & 1)) {
+      if (lane == 0 && warp_live) {
+        tma_store_2d(&maps.e[2], a_stage, n0 - 32, m0w, pol_keep);
+        bulk_commit();
+      }
+      if (m < g.M) e.ss_out[static_cast<size_t>(m) * (g.resid_n / 64) + (n0 - 32) / 64] = ss;
+      ss = 0.f;
+    }
+  }
+  if (lane == 0) {
+    bulk_commit();
+    bulk_wait_read_all();  // the boxes are read before the CTA's shared memory goes
+  }
+  __syncwarp();
+  return true;
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g) {
@@ -503,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_tfull = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto bar_tempty = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t bar_drain = bar0 + 8u * (2 * S + 4);
+  const uint32_t bar_res0 = bar0 + 8u * (2 * S + 5);  // residual boxes landed, one per stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -517,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_tempty(a), kEpiThreads);
     }
     mbar_init(bar_drain, 1);
+    for (int f = 0; f < 4; ++f) mbar_init(bar_res0 + 8u * f, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -525,6 +734,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&maps.b[0]);
     tma_prefetch_map(&maps.b[1]);
     tma_prefetch_map(&maps.b[2]);
+    if (EPI == kEpiResid) {
+      tma_prefetch_map(&maps.e[0]);
+      tma_prefetch_map(&maps.e[1]);
+      tma_prefetch_map(&maps.e[2]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), C::kTmemCols);
@@ -595,10 +809,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       PDS_GEMM_TRACE_HOOK(cta, 1);
       SegIter si{it0, it1, g.kb};
       int unit, k0, k1;
+      int mt = 0, nt = 0;
       bool ok = true;
       while (ok && si.next(unit, k0, k1)) {
-        int mt, nt;
         unit_tile(g, unit, rank, mt, nt);
+        // the last tile's residual, on its way to L2 while the tile is computed
+        if (EPI == kEpiResid && si.it >= si.end)
+          for (int b = 0; b < C::kResBoxes; ++b)
+            tma_prefetch_l2_2d(&maps.e[0], nt * BN + b * 32, mt * BM);
         for (int kb = k0; kb < k1; ++kb) {
           const int s = issued % S;
           if (issued >= npre) {
@@ -612,6 +830,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sbase + s * C::kStage, &maps.a, bar_full(s), kb * BK, mt * BM, pol_a);
           ++issued;
         }
+      }
+      // The last tile's residual, into the stages as the last MMAs free them
+      // (continuing the ring as if they were further k-blocks).  A split
+      // tile's residual is loaded too: this CTA may be the one to finish it.
+      if (EPI == kEpiResid && ok && it1 > it0) {
+        const uint64_t pol_r = policy_evict_first();  // the residual's last read
+        int issued_res = 0;
+        for (int f = 0; f < C::kResStages; ++f) {
+          const int v = issued + f;
+          const int s = v % S;
+          if (v >= S && !mbar_wait(bar_empty(s), ((v / S) & 1) ^ 1, abort_flag, g.status)) break;
+          const int nb = min(C::kBoxesPerStage, C::kResBoxes - f * C::kBoxesPerStage);
+          mbar_arrive_expect_tx(bar_res0 + 8u * f, static_cast<uint32_t>(nb) * 16384u);
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d(sbase + s * C::kStage + b * 16384u, &maps.e[0], bar_res0 + 8u * f,
+                        nt * BN + (f * C::kBoxesPerStage + b) * 32, mt * BM, pol_r);
+          ++issued_res;
+        }
+        // none of these copies may still be landing when the CTA exits,
+        // whether or not the epilogue uses them
+        for (int f = 0; f < issued_res; ++f)
+          if (!mbar_wait(bar_res0 + 8u * f, 0, abort_flag, g.status)) break;
       }
     }
   } else if (warp == 1) {
@@ -681,7 +921,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) PDS_GEMM_TRACE_HOOK(cta, 4);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_grp * 32) << 16) + ab * BN;
       const int tile = mt + nt * g.tiles_m;
-      const int m = mt * BM + row;
       Fixup fx{false, 0, 0, grp, rank, unit};
       bool run = true;
       if (!(k0 == 0 && k1 == g.kb)) {
@@ -714,8 +953,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (run) {
-        run_epilogue<BN, EPI>(g, taddr, fx, mt, nt, row, ch, lane, rscale, st);
-        if (fx.active && leader) g.counters[tile] = 0;
+        const bool last = si.it >= si.end;
+        const bool split = fx.active;
+        // The CTA's last tile: a split one is finished in TMEM through the
+        // drained stages, then the epilogue reads TMEM as for an unsplit tile.
+        // (Residual GEMMs only: in the others it costs registers in every
+        // epilogue path, and their schedules seldom split a last tile.)
+        if constexpr (EPI == kEpiResid) {
+          if (split && last) {
+            fixup_reduce_smem<BN, EPI>(g, fx, taddr, nt, row, ch, sbase, it1 - it0,
+                                       C::kResBoxes);
+            fx.active = false;
+          }
+        }
+        if (EPI == kEpiResid && last) {
+          if (!resid_epilogue_smem<BN>(g, maps, taddr, mt, nt, row, ch, lane, sbase, it1 - it0,
+                                       bar_res0, abort_flag, st,
+                                       reinterpret_cast<float*>(smem + S * C::kStage + 1024)))
+            break;
+        } else {
+          run_epilogue<BN, EPI>(g, taddr, fx, mt, nt, row, ch, lane, rscale, st);
+        }
+        if (split && leader) g.counters[tile] = 0;
       }
       if (leader) PDS_GEMM_TRACE_HOOK(cta, 5);
       tc_fence_before();
@@ -765,15 +1024,17 @@ EncodeTiledFn encode_fn() {
 struct TmapKey {
   const void* p;
   uint64_t inner, outer;
-  uint32_t box_rows;
+  uint32_t box_inner, box_rows, elem_bytes;
   bool operator==(const TmapKey& o) const {
-    return p == o.p && inner == o.inner && outer == o.outer && box_rows == o.box_rows;
+    return p == o.p && inner == o.inner && outer == o.outer && box_inner == o.box_inner &&
+           box_rows == o.box_rows && elem_bytes == o.elem_bytes;
   }
 };
 struct TmapKeyHash {
   size_t operator()(const TmapKey& k) const {
     return std::hash<const void*>()(k.p) ^ (k.inner * 0x9E3779B97F4A7C15ull) ^ (k.outer << 20) ^
-           (static_cast<size_t>(k.box_rows) << 44);
+           (static_cast<size_t>(k.box_rows) << 44) ^ (static_cast<size_t>(k.box_inner) << 32) ^
+           (static_cast<size_t>(k.elem_bytes) << 56);
   }
 };
 struct TmapCache {
@@ -786,11 +1047,13 @@ void tmap_cache_destroy(TmapCache* c) { delete c; }
 
 namespace {
 
-// bf16 matrix [outer rows, inner columns], box of 64 columns x box_rows rows,
-// 128-byte swizzle.
+// Row-major matrix [outer rows, inner columns] of bf16 (elem_bytes 2) or
+// float32 (4), box of box_inner columns (128 bytes) x box_rows rows, 128-byte
+// swizzle.  The default is the GEMM operand box: 64 bf16 columns x 128 rows.
 pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner, uint64_t outer,
-                   std::string* err, uint32_t box_rows = 128) {
-  TmapKey key{p, inner, outer, box_rows};
+                   std::string* err, uint32_t box_rows = 128, uint32_t elem_bytes = 2) {
+  const uint32_t box_inner = 128u / elem_bytes;
+  TmapKey key{p, inner, outer, box_inner, box_rows, elem_bytes};
   if (c.maps) {
     std::lock_guard<std::mutex> g(c.maps->mu);
     auto it = c.maps->maps.find(key);
@@ -805,10 +1068,12 @@ pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner
     return PDS_ELAUNCH;
   }
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  const cuuint64_t strides[1] = {inner * elem_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, box,
+  const CUtensorMapDataType dt =
+      elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(out, dt, 2, const_cast<void*>(p), dims, strides, box,
                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -866,15 +1131,26 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   // reducing and re-reading partial tiles.  Fewer CTAs without splits often win.
   // A single row tile streams every weight byte once: there the bandwidth of
   // all SMs matters more than splits, so every group is used.
+  // A 128-wide tile moves two thirds of the shared-memory bytes of a 256-wide
+  // one per k-block, and its k-blocks take about that much less time.
+  const double kb_us = bn == 256 ? 0.35 : 0.24;
+  // PDS_GEMM_SPLIT_US="a,b" replaces the split penalty a + b per extra
+  // contributor (a tuning knob).
+  static const std::pair<double, double> split_us = [] {
+    const char* v = std::getenv("PDS_GEMM_SPLIT_US");
+    double a = 4.0, b = 5.0;
+    if (v) std::sscanf(v, "%lf,%lf", &a, &b);
+    return std::make_pair(a, b);
+  }();
   double best = 1e30;
   int best_g = gmax;
   for (int gr = gmax; g.tiles_m > 1 && gr >= std::max(1, gmax / 3); --gr) {
     const double per = static_cast<double>(g.total) / gr;
-    double cost = std::ceil(per) * 0.35;
+    double cost = std::ceil(per) * kb_us;
     if (g.units % gr != 0) {
       const bool aligned = g.total % gr == 0 && (g.kb % static_cast<int>(per) == 0);
       const double contrib = g.kb / per + (aligned ? 0.0 : 1.0);
-      cost += 4.0 + 5.0 * std::max(0.0, contrib - 1.0);
+      cost += split_us.first + split_us.second * std::max(0.0, contrib - 1.0);
     }
     if (cost < best - 1e-9) {
       best = cost;
@@ -975,7 +1251,7 @@ pds_status tc_gemm_plain(TcContext& c, const uint16_t* A, const uint16_t* W, flo
   g.c_out = Cout;
   g.ldc = N;
   make_schedule(g, c, M, N / bn, K, bn);
-  GemmMaps maps;
+  GemmMaps maps{};
   pds_status rc;
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
   if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, bn))) != PDS_OK) return rc;
@@ -987,18 +1263,31 @@ pds_status tc_gemm_plain(TcContext& c, const uint16_t* A, const uint16_t* W, flo
 
 pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int M, int N, int K,
                          const ResidEpilogue& e, cudaStream_t st, std::string* err) {
-  const int bn = N % 256 == 0 ? 256 : 128;
+  // PDS_GEMM_BN_RESID=128 forces 128-wide tiles (a tuning knob).
+  static const int env_bn = [] {
+    const char* v = std::getenv("PDS_GEMM_BN_RESID");
+    return v ? std::atoi(v) : 256;
+  }();
+  const int bn = (N % 256 == 0 && env_bn != 128) ? 256 : 128;
   GemmArgs g{};
   g.wrows0 = N;
   g.resid = e;
   g.resid_n = N;
   make_schedule(g, c, M, N / bn, K, bn);
-  GemmMaps maps;
+  GemmMaps maps{};
   pds_status rc;
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
   if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, bn))) != PDS_OK) return rc;
   maps.b[1] = maps.b[0];
   maps.b[2] = maps.b[0];
+  // residual in (whole-tile-high boxes), h and a out (one warp's 32 rows)
+  if ((rc = get_map(c, &maps.e[0], e.resid, N, M, err, 128, 4)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.e[1], e.out, N, M, err, 32, 4)) != PDS_OK) return rc;
+  if (e.gain) {
+    if ((rc = get_map(c, &maps.e[2], e.a_out, N, M, err, 32, 2)) != PDS_OK) return rc;
+  } else {
+    maps.e[2] = maps.e[1];
+  }
   return bn == 256 ? launch<256, kEpiResid>(c, maps, g, st, err)
                    : launch<128, kEpiResid>(c, maps, g, st, err);
 }
@@ -1009,7 +1298,7 @@ pds_status tc_gemm_swiglu(TcContext& c, const uint16_t* A, const WeightRows& W, 
   g.pair_mode = 1;
   g.swiglu = e;
   make_schedule(g, c, M, e.ffn / 128, K, 256);
-  GemmMaps maps;
+  GemmMaps maps{};
   pds_status rc;
   const uint32_t br = weight_box_rows(g, 256);
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
@@ -1029,7 +1318,7 @@ pds_status tc_gemm_qkv(TcContext& c, const uint16_t* A, const WeightRows& W, int
   // 256-column tiles always (each 128-column half holds whole heads); a
   // last half past N reads zero rows and is skipped by the epilogue.
   make_schedule(g, c, M, (N + 255) / 256, K, 256);
-  GemmMaps maps;
+  GemmMaps maps{};
   pds_status rc;
   const uint32_t br = weight_box_rows(g, 256);
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
@@ -1123,7 +1412,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   g.ldc = N;
   make_schedule(g, c, M, N / kNoAllocBN, K, kNoAllocBN, grid_cap);
   g.cs = 1;  // a plain launch, without clusters
-  GemmMaps maps;
+  GemmMaps maps{};
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
   if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, kNoAllocBN))) != PDS_OK)
     return rc;
