@@ -23,7 +23,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return uint32_t(f32_to_bf16(lo)) | (uint32_t(f32_to_bf16(hi)) << 16);
 }
 
-__device__ __forceinline__ float silu(float t) { return t / (1.0f + __expf(-t)); }
+__device__ __forceinline__ float silu(float t) { return __fdividef(t, 1.0f + __expf(-t)); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -82,6 +82,10 @@ struct GemmArgs {
   // The CTAs of a group run as clusters of cs (1, 2 or 4): each loads 1/cs
   // of the shared weight tile and multicasts it to the whole cluster.
   int cs;
+  // Pair mode (cs = 2): the two CTAs of a cluster compute a 256 x BN tile
+  // with cta_group::2 MMAs, each loading its own 128 rows of A and half of
+  // the BN weight rows (no multicast).
+  int pair;
   int wrows0, wrows1;  // rows of weight blocks 0 and 1 (concatenated along N)
   int pair_mode;       // W tile = 128 rows of block 0 then the same rows of block 1
   uint32_t* status;
@@ -95,11 +99,14 @@ struct GemmArgs {
   QkvEpilogue qkv;
 };
 
-template <int BN>
+// PAIR: the CTA is one of a pair that computes a 256 x BN tile with
+// cta_group::2 MMAs; it holds its own 128 rows of A and half of W's BN rows.
+template <int BN, bool PAIR = false>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr int kStages = PAIR ? 6 : (BN == 256 ? 4 : 6);
   static constexpr uint32_t kABytes = BM * BK * 2;
-  static constexpr uint32_t kBBytes = BN * BK * 2;
+  static constexpr uint32_t kBBytes = kBRows * BK * 2;
   static constexpr uint32_t kStage = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
   static constexpr int kBars = 2 * kStages + 5 + 4;
@@ -175,14 +182,20 @@ struct Fixup {
   int gf, gl, me, r, unit;
 };
 
-// Warp 0 is the TMA producer, warp 1 the MMA issuer (and TMEM owner).
-// Epilogue threads: warps 2..9.  Warp w reads TMEM lanes 32*(w%4).. (one
-// output row per thread) and takes half of the tile's columns (ch = 0 for
-// warps 2..5, 1 for warps 6..9), so two threads share each row.
+// Warpgroup 0: warp 0 is the TMA producer, warp 1 the MMA issuer (and TMEM
+// owner), warps 2 and 3 idle.  Epilogue threads: warpgroups 1 and 2 (warps
+// 4..11).  Warp w reads TMEM lanes 32*(w%4).. (one output row per thread)
+// and takes half of the tile's columns (ch = 0 for warps 4..7, 1 for warps
+// 8..11), so two threads share each row.  Warpgroup 0 gives registers to
+// the epilogue (setmaxnreg): the launch's 168 per thread become 72 and 216.
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kEpiFirstThread = 64;
+constexpr int kEpiFirstThread = 128;
 constexpr int kThreads = kEpiFirstThread + kEpiThreads;
+constexpr int kRegsControl = 88;
+constexpr int kRegsEpilogue = 208;
+static_assert(128 * kRegsControl + kEpiThreads * kRegsEpilogue <= kThreads * 168,
+              "register split within the launch's allocation");
 
 // Partial tile of rank r of group grp for unit u: slot 0 if u is the group's
 // first unit (its range starts inside u), else slot 1 (u is its last).
@@ -193,79 +206,15 @@ __device__ __forceinline__ const float4* partial_slot(const GemmArgs& g, int grp
          static_cast<size_t>((grp * g.gs + r) * 2 + slot) * (BM * BN / 4);
 }
 
-// Half h (16 columns) of chunk j of this thread's row: the TMEM
-// accumulator, plus the partial tiles of the other CTAs of a split tile,
-// summed in CTA order (so in k order, whoever reduces).  Two contributors'
-// loads are in flight at once.
-template <int BN>
-__device__ __forceinline__ void acc_sub(const GemmArgs& g, uint32_t taddr, const Fixup& fx,
-                                        int j, int h, int row, float (&v)[16]) {
-  if (!fx.active) {
-    sm100::tmem_load16(taddr + j * 32 + h * 16, v);
-    return;
-  }
-  float own[16];
-  const int q0 = j * 8 + h * 4;
-  for (int c0 = fx.gf; c0 <= fx.gl; c0 += 2) {
-    const int c1 = c0 + 1;
-    const bool has1 = c1 <= fx.gl;
-    const bool ld0 = c0 != fx.me, ld1 = has1 && c1 != fx.me;
-    float4 b0[4], b1[4];
-    // the partial loads go out before the TMEM load, which orders memory
-    if (ld0) {
-      const float4* p = partial_slot(g, c0, fx.r, fx.unit, BN) + q0 * BM + row;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) b0[q] = __ldcg(p + q * BM);
-    }
-    if (ld1) {
-      const float4* p = partial_slot(g, c1, fx.r, fx.unit, BN) + q0 * BM + row;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) b1[q] = __ldcg(p + q * BM);
-    }
-    if (c0 == fx.gf) {
-      sm100::tmem_load16(taddr + j * 32 + h * 16, own);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 x = ld0 ? b0[q] : make_float4(own[4 * q], own[4 * q + 1], own[4 * q + 2],
-                                                 own[4 * q + 3]);
-      v[4 * q] += x.x;
-      v[4 * q + 1] += x.y;
-      v[4 * q + 2] += x.z;
-      v[4 * q + 3] += x.w;
-    }
-    if (has1) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 x = ld1 ? b1[q] : make_float4(own[4 * q], own[4 * q + 1], own[4 * q + 2],
-                                                   own[4 * q + 3]);
-        v[4 * q] += x.x;
-        v[4 * q + 1] += x.y;
-        v[4 * q + 2] += x.z;
-        v[4 * q + 3] += x.w;
-      }
-    }
-  }
-}
-
 // Warp-private staging tile of 32 rows x 128 bytes in shared memory, 16-byte
 // chunks XOR-swizzled by row, so that a thread-per-row write and a
 // four-rows-per-instruction read are both free of bank conflicts.  It turns
 // the TMEM layout (one row per thread) into row-contiguous global accesses.
 // Two 16-column pieces (chunk ja half ha, chunk jb half hb) of this thread's
 // row; without a split the two TMEM loads share one wait.
-template <int BN>
-__device__ __forceinline__ void acc_pair(const GemmArgs& g, uint32_t taddr, const Fixup& fx,
-                                         int ja, int ha, int jb, int hb, int row, float (&va)[16],
-                                         float (&vb)[16]) {
-  if (!fx.active) {
-    sm100::tmem_load16x2(taddr + ja * 32 + ha * 16, taddr + jb * 32 + hb * 16, va, vb);
-    return;
-  }
-  acc_sub<BN>(g, taddr, fx, ja, ha, row, va);
-  acc_sub<BN>(g, taddr, fx, jb, hb, row, vb);
+__device__ __forceinline__ void acc_pair(uint32_t taddr, int ja, int ha, int jb, int hb,
+                                         float (&va)[16], float (&vb)[16]) {
+  sm100::tmem_load16x2(taddr + ja * 32 + ha * 16, taddr + jb * 32 + hb * 16, va, vb);
 }
 
 // x^2 + y^2 + z^2 + w^2 with a fixed rounding order (no contraction), so
@@ -346,9 +295,8 @@ __device__ __forceinline__ bool chunk_exists(const GemmArgs& g, int nt, int j) {
 // The fused epilogue of one tile for this thread (row `row` of the tile,
 // column half `ch`); r is the row's RMSNorm scale (SwiGLU and QKV).
 template <int BN, int EPI>
-__device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, const Fixup& fx,
-                                             int mt, int nt, int row, int ch, int lane, float r,
-                                             const Stage& st) {
+__device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, int mt, int nt,
+                                             int row, int ch, int lane, float r, const Stage& st) {
   const int m = mt * BM + row;
   const bool live = m < g.M;
   const int m0w = mt * BM + (row & ~31);            // first row of this warp's 32
@@ -380,7 +328,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
       }
       {
         float v0[16], v1[16];
-        acc_pair<BN>(g, taddr, fx, j, 0, j, 1, row, v0, v1);
+        acc_pair(taddr, j, 0, j, 1, v0, v1);
         stage_f32(st, lane, 0, v0);
         stage_f32(st, lane, 4, v1);
       }
@@ -437,7 +385,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float gv[16], uv[16];
-        acc_pair<BN>(g, taddr, fx, jg, h, 4 + jg, h, row, gv, uv);
+        acc_pair(taddr, jg, h, 4 + jg, h, gv, uv);
 #pragma unroll
         for (int k = 0; k < 16; ++k) gv[k] = silu(r * gv[k]) * (r * uv[k]);
         stage_bf16(st, lane, 2 * h, gv);
@@ -457,7 +405,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
 #pragma unroll 1
       for (int jj = 0; jj < 4; ++jj) {
         float v0[16], v1[16];
-        acc_pair<BN>(g, taddr, fx, ch * 4 + jj, 0, ch * 4 + jj, 1, row, v0, v1);
+        acc_pair(taddr, ch * 4 + jj, 0, ch * 4 + jj, 1, v0, v1);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           v0[k] *= r;
@@ -487,7 +435,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           float va[16], vb[16];
-          acc_pair<BN>(g, taddr, fx, ch * 4 + ja, h, ch * 4 + jb, h, row, va, vb);
+          acc_pair(taddr, ch * 4 + ja, h, ch * 4 + jb, h, va, vb);
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const float2 sc = __ldg(cs + static_cast<size_t>(i0 + 16 * h + k) * e.rope_ld);
@@ -508,12 +456,64 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
 // Shared-memory address of epilogue box b of a CTA's last tile: the boxes
 // fill the stages in the order the ring frees them after the CTA's n_it
 // k-blocks, kBoxesPerStage to a stage.
-template <int BN>
+template <int BN, bool PAIR>
 __device__ __forceinline__ uint32_t epi_box(uint32_t sbase, int n_it, int b) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   const int s = (n_it + b / C::kBoxesPerStage) % C::kStages;
   return sbase + static_cast<uint32_t>(s) * C::kStage +
          static_cast<uint32_t>(b % C::kBoxesPerStage) * 16384u;
+}
+
+// Finishes a split tile in TMEM from registers: for each 32-column chunk
+// this thread's epilogue reads, the contributors' accumulators are summed
+// in k order from zero (its own TMEM value in its place) and written back.
+// Two contributors' partial rows are in flight at once.
+template <int BN, int EPI>
+__device__ __forceinline__ void fixup_reduce_regs(const GemmArgs& g, const Fixup& fx,
+                                                  uint32_t taddr, int nt, int row, int ch) {
+  using namespace sm100;
+  constexpr int kOwned = owned_chunks<BN, EPI>();
+#pragma unroll 1
+  for (int i = 0; i < kOwned; ++i) {
+    const int j = owned_chunk<BN, EPI>(ch, i);
+    if (!chunk_exists<BN, EPI>(g, nt, j)) continue;
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) v[q] = 0.f;
+#pragma unroll 1
+    for (int c0 = fx.gf; c0 <= fx.gl; c0 += 2) {
+      float4 b[2][8];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = c0 + u;
+        if (c <= fx.gl && c != fx.me) {
+          const float4* p = partial_slot(g, c, fx.r, fx.unit, BN) + static_cast<size_t>(j * 8) * BM + row;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) b[u][q] = __ldcg(p + q * BM);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = c0 + u;
+        if (c > fx.gl) break;
+        if (c == fx.me) {
+          float own[32];
+          tmem_load32(taddr + j * 32, own);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] += own[q];
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            v[4 * q] += b[u][q].x;
+            v[4 * q + 1] += b[u][q].y;
+            v[4 * q + 2] += b[u][q].z;
+            v[4 * q + 3] += b[u][q].w;
+          }
+        }
+      }
+    }
+    tmem_store32(taddr + j * 32, v);
+  }
 }
 
 // Finishes a split tile that this CTA completes as its last tile, in TMEM:
@@ -523,7 +523,7 @@ __device__ __forceinline__ uint32_t epi_box(uint32_t sbase, int n_it, int b) {
 // thread copies only its own row of the other contributors' partial tiles
 // (cp.async, one copy ahead, two buffers per column half in the drained
 // stages from box `box0` on), so no thread waits for another.
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup& fx,
                                                   uint32_t taddr, int nt, int row, int ch,
                                                   uint32_t sbase, int n_it, int box0) {
@@ -535,7 +535,7 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
   auto issue = [&](int k) {
     const int i = k / nother, t = k - (k / nother) * nother;
     const int j = owned_chunk<BN, EPI>(ch, i);
-    const uint32_t dst = epi_box<BN>(sbase, n_it, box0 + ch * 2 + (k & 1)) +
+    const uint32_t dst = epi_box<BN, PAIR>(sbase, n_it, box0 + ch * 2 + (k & 1)) +
                          static_cast<uint32_t>(row) * 16u;
     const float4* src = partial_slot(g, contributor(t), fx.r, fx.unit, BN) +
                         static_cast<size_t>(j * 8) * BM + row;
@@ -576,7 +576,7 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
       } else {
         asm volatile("cp.async.wait_group 0;" ::: "memory");
       }
-      const uint32_t pb = epi_box<BN>(sbase, n_it, box0 + ch * 2 + (k & 1)) +
+      const uint32_t pb = epi_box<BN, PAIR>(sbase, n_it, box0 + ch * 2 + (k & 1)) +
                           static_cast<uint32_t>(row) * 16u;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -600,14 +600,14 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
 // each warp then stores its 32 rows of each box with TMA.  No global load
 // or store of a tile element goes through registers.  Returns false if a
 // wait gave up.
-template <int BN>
+template <int BN, bool PAIR>
 __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const GemmMaps& maps,
                                                     uint32_t taddr, int mt, int nt, int row,
                                                     int ch, int lane, uint32_t sbase, int n_it,
                                                     uint32_t bar_res0, volatile int* abort_flag,
                                                     const Stage& st, float* gain_sm) {
   using namespace sm100;
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   constexpr int EPI = kEpiResid;  // for the trace hook
   (void)EPI;
   constexpr int kChunks = BN / 64;  // 32-column chunks of this thread's half
@@ -636,7 +636,7 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
     if (c == 0 && row == 0 && ch == 0) PDS_GEMM_TRACE_HOOK(blockIdx.x, 7);
     float v[32];
     tmem_load32(taddr + j * 32, v);
-    const uint32_t rrow = epi_box<BN>(sbase, n_it, j) + static_cast<uint32_t>(row) * 128u;
+    const uint32_t rrow = epi_box<BN, PAIR>(sbase, n_it, j) + static_cast<uint32_t>(row) * 128u;
     if (e.gain && (c & 1) == 0 && c > 0) {
       // the previous pair's operand store has read the staging area
       if (lane == 0) bulk_wait_read_all();
@@ -671,7 +671,7 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && warp_live)
-      tma_store_2d(&maps.e[1], epi_box<BN>(sbase, n_it, j) + lane_grp * 4096u, n0, m0w, pol_keep);
+      tma_store_2d(&maps.e[1], epi_box<BN, PAIR>(sbase, n_it, j) + lane_grp * 4096u, n0, m0w, pol_keep);
     if (e.gain && (j & 1)) {
       if (lane == 0 && warp_live) {
         tma_store_2d(&maps.e[2], a_stage, n0 - 32, m0w, pol_keep);
@@ -689,13 +689,13 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
   return true;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g) {
   using namespace sm100;
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   constexpr int S = C::kStages;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+  constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -718,11 +718,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), g.cs);  // freed by the MMAs of every CTA of the cluster
+      // freed by the MMAs of every CTA of a multicast cluster; a pair's
+      // stages are freed by the even CTA's MMAs alone
+      mbar_init(bar_empty(s), PAIR ? 1 : g.cs);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
-      mbar_init(bar_tempty(a), kEpiThreads);
+      // one arrival per epilogue warp (of both CTAs of a pair)
+      mbar_init(bar_tempty(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(bar_drain, 1);
     for (int f = 0; f < 4; ++f) mbar_init(bar_res0 + 8u * f, 1);
@@ -741,8 +744,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(misc), C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(misc), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(misc), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -751,6 +759,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (g.cs > 1) cluster_sync();
   const uint32_t tmem_base = misc[0];
   const uint16_t cmask = static_cast<uint16_t>((1u << g.cs) - 1);
+  // A pair: rank 0 issues the MMAs and owns the stage-full and
+  // accumulator-empty barriers both CTAs' copies and epilogues signal.
+  const uint32_t prank = PAIR ? cluster_rank() : 0u;
   if (threadIdx.x == 0) PDS_GEMM_TRACE_HOOK(cta, 0);
 
   // Everything above overlaps the previous kernel when launched with
@@ -766,7 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int issued = 0;  // producer: k-block loads issued
   int consumed = 0;
 
+  // Each role changes its registers first thing, so that its code is
+  // compiled for its own register count (warps 0..3 lower theirs, the
+  // epilogue warpgroups take them).
   if (warp == 0) {
+    setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
       // A (activations) is re-read by every column tile: keep it.  A weight
       // box is read once when one cluster holds all the row tiles of its
@@ -775,9 +790,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_a = policy_evict_last();
       const uint64_t pol_w = g.cs == g.gs ? policy_evict_first() : policy_evict_normal();
       const int slice = BN / g.cs;  // weight rows this CTA loads for the cluster
-      const int r0 = (g.cs > 1 ? static_cast<int>(cluster_rank()) : 0) * slice;
+      const int r0 = (g.cs > 1 && !PAIR ? static_cast<int>(cluster_rank()) : 0) * slice;
+      // where a stage's copies complete: the pair leader's barrier, or our own
+      auto full_bar = [&](int s) { return PAIR ? mapa_shared(bar_full(s), 0) : bar_full(s); };
       auto load_w = [&](int s, int nt, int kb) {
-        if (g.cs == 1) {
+        if constexpr (PAIR) {
+          // this CTA's half of the pair's BN weight rows
+          int mi, row;
+          b_source<BN>(g, nt, static_cast<int>(prank), mi, row);
+          tma_load_2d_pair(sbase + s * C::kStage + C::kABytes, &maps.b[mi], full_bar(s), kb * BK,
+                           row, pol_w);
+        } else if (g.cs == 1) {
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h) {
             int mi, row;
@@ -800,7 +823,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           int mt, nt;
           unit_tile(g, unit, rank, mt, nt);
           for (int kb = k0; kb < k1 && n < npre; ++kb, ++n) {
-            mbar_arrive_expect_tx(bar_full(n), C::kStage);
+            // the pair leader expects both CTAs' bytes
+            if (prank == 0) mbar_arrive_expect_tx(bar_full(n), PAIR ? 2 * C::kStage : C::kStage);
             load_w(n, nt, kb);
           }
         }
@@ -824,10 +848,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(bar_full(s), C::kStage);
+            if (prank == 0) mbar_arrive_expect_tx(bar_full(s), PAIR ? 2 * C::kStage : C::kStage);
             load_w(s, nt, kb);
           }
-          tma_load_2d(sbase + s * C::kStage, &maps.a, bar_full(s), kb * BK, mt * BM, pol_a);
+          if constexpr (PAIR) {
+            tma_load_2d_pair(sbase + s * C::kStage, &maps.a, full_bar(s), kb * BK, mt * BM, pol_a);
+          } else {
+            tma_load_2d(sbase + s * C::kStage, &maps.a, bar_full(s), kb * BK, mt * BM, pol_a);
+          }
           ++issued;
         }
       }
@@ -855,7 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    setmaxnreg_dec<kRegsControl>();
+    if (lane == 0 && prank == 0) {
       SegIter si{it0, it1, g.kb};
       int tile, k0, k1, sg = 0;
       bool ok = true;
@@ -876,9 +905,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t ad = smem_desc_sw128(a_addr);
           const uint64_t bd = smem_desc_sw128(a_addr + C::kABytes);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, (kb > k0 || k > 0) ? 1u : 0u);
-          if (g.cs > 1) {
+          for (int k = 0; k < BK / 16; ++k) {
+            if constexpr (PAIR) {
+              umma_bf16_pair(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, (kb > k0 || k > 0) ? 1u : 0u);
+            } else {
+              umma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, (kb > k0 || k > 0) ? 1u : 0u);
+            }
+          }
+          if constexpr (PAIR) {
+            umma_commit_pair_mc(bar_empty(s), 0x3);  // the stage is free in both CTAs
+          } else if (g.cs > 1) {
             umma_commit_mc(bar_empty(s), cmask);  // the stage is free in every CTA's view
           } else {
             umma_commit(bar_empty(s));
@@ -886,20 +922,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++consumed;
         }
         if (!ok) break;
-        umma_commit(bar_tfull(ab));
+        if constexpr (PAIR) {
+          umma_commit_pair_mc(bar_tfull(ab), 0x3);  // both halves of the accumulator
+        } else {
+          umma_commit(bar_tfull(ab));
+        }
         PDS_GEMM_TRACE_HOOK(cta, 3);
         ++sg;
       }
       // Every MMA this thread issued has completed before TMEM is released.
-      umma_commit(bar_drain);
+      if constexpr (PAIR) {
+        umma_commit_pair(bar_drain);
+      } else {
+        umma_commit(bar_drain);
+      }
       int dummy_abort = 0;
       mbar_wait(bar_drain, 0, &dummy_abort, g.status);
     }
-  } else {
-    const Stage st{reinterpret_cast<float4*>(smem + S * C::kStage + C::kMiscBytes) +
-                   (warp - 2) * 256};
-    const int lane_grp = warp & 3;   // this warp's TMEM lanes: 32*lane_grp ..
-    const int ch = (warp - 2) >> 2;  // which half of the tile's columns
+  } else if (warp >= kEpiFirstThread / 32) {
+    setmaxnreg_inc<kRegsEpilogue>();
+    const int ew = warp - kEpiFirstThread / 32;  // epilogue warp 0..7
+    const Stage st{reinterpret_cast<float4*>(smem + S * C::kStage + C::kMiscBytes) + ew * 256};
+    const int lane_grp = warp & 3;  // this warp's TMEM lanes: 32*lane_grp ..
+    const int ch = ew >> 2;         // which half of the tile's columns
     const int row = lane_grp * 32 + lane;
     const bool leader = threadIdx.x == kEpiFirstThread;
     grid_dep_wait();
@@ -955,32 +1000,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (run) {
         const bool last = si.it >= si.end;
         const bool split = fx.active;
-        // The CTA's last tile: a split one is finished in TMEM through the
-        // drained stages, then the epilogue reads TMEM as for an unsplit tile.
-        // (Residual GEMMs only: in the others it costs registers in every
-        // epilogue path, and their schedules seldom split a last tile.)
-        if constexpr (EPI == kEpiResid) {
-          if (split && last) {
-            fixup_reduce_smem<BN, EPI>(g, fx, taddr, nt, row, ch, sbase, it1 - it0,
-                                       C::kResBoxes);
-            fx.active = false;
+        // A split tile is first finished in TMEM (the other contributors'
+        // partials added in k order), then the epilogue reads TMEM as for an
+        // unsplit tile.  The CTA's last tile stages the partials in the
+        // drained stages (after the residual boxes of a residual GEMM).
+        if (split) {
+          if (last) {
+            fixup_reduce_smem<BN, EPI, PAIR>(g, fx, taddr, nt, row, ch, sbase, it1 - it0,
+                                             EPI == kEpiResid ? C::kResBoxes : 0);
+          } else {
+            fixup_reduce_regs<BN, EPI>(g, fx, taddr, nt, row, ch);
           }
+          fx.active = false;
         }
         if (EPI == kEpiResid && last) {
-          if (!resid_epilogue_smem<BN>(g, maps, taddr, mt, nt, row, ch, lane, sbase, it1 - it0,
+          if (!resid_epilogue_smem<BN, PAIR>(g, maps, taddr, mt, nt, row, ch, lane, sbase, it1 - it0,
                                        bar_res0, abort_flag, st,
                                        reinterpret_cast<float*>(smem + S * C::kStage + 1024)))
             break;
         } else {
-          run_epilogue<BN, EPI>(g, taddr, fx, mt, nt, row, ch, lane, rscale, st);
+          run_epilogue<BN, EPI>(g, taddr, mt, nt, row, ch, lane, rscale, st);
         }
         if (split && leader) g.counters[tile] = 0;
       }
       if (leader) PDS_GEMM_TRACE_HOOK(cta, 5);
+      // this warp's TMEM reads are done: one arrival per warp, on the pair
+      // leader's barrier for a pair
       tc_fence_before();
-      mbar_arrive(bar_tempty(ab));
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR && prank != 0) {
+          mbar_arrive_cluster(mapa_shared(bar_tempty(ab), 0));
+        } else {
+          mbar_arrive(bar_tempty(ab));
+        }
+      }
       ++sg;
     }
+  } else {
+    setmaxnreg_dec<kRegsControl>();  // warps 2 and 3: only their registers are needed
   }
 
   // On a timeout the producer may have loads in flight: give them time to
@@ -996,7 +1054,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // no CTA leaves while a peer may still multicast into it or arrive on it
   if (g.cs > 1) cluster_sync();
   if (threadIdx.x == 0) PDS_GEMM_TRACE_HOOK(cta, 6);
-  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (warp == 1) {
+    if constexpr (PAIR) {
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    } else {
+      tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+  }
 }
 
 // ------------------------------------------------------------ host side
@@ -1089,11 +1153,11 @@ pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner
 
 // Rows of a weight box: the slice one CTA of a cluster loads.
 uint32_t weight_box_rows(const GemmArgs& g, int bn) {
-  return g.cs > 1 ? static_cast<uint32_t>(bn / g.cs) : 128u;
+  return g.cs > 1 && !g.pair ? static_cast<uint32_t>(bn / g.cs) : 128u;
 }
 
 void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, int bn,
-                   int max_grid = kGemmMaxGrid) {
+                   int max_grid = kGemmMaxGrid, bool allow_pair = true) {
   g.M = M;
   g.K = K;
   g.tiles_m = (M + BM - 1) / BM;
@@ -1112,12 +1176,25 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
     const char* v = std::getenv("PDS_GEMM_CLUSTER");
     return v ? std::max(1, std::atoi(v)) : 4;
   }();
+  // Pair mode for 256-wide tiles whenever the group holds whole pairs of
+  // row tiles: it halves the weight bytes each SM takes in per k-block.
+  // PDS_GEMM_PAIR=0 turns it off (a tuning knob).
+  static const bool env_pair = [] {
+    const char* v = std::getenv("PDS_GEMM_PAIR");
+    return !(v && std::atoi(v) == 0);
+  }();
   g.cs = 1;
-  for (int cs = 4; cs >= 2; cs /= 2)
-    if (cs <= env_cs && gs % cs == 0 && bn / cs >= 64) {
-      g.cs = cs;
-      break;
-    }
+  g.pair = 0;
+  if (env_pair && bn == 256 && gs % 2 == 0 && allow_pair) {
+    g.pair = 1;
+    g.cs = 2;
+  } else {
+    for (int cs = 4; cs >= 2; cs /= 2)
+      if (cs <= env_cs && gs % cs == 0 && bn / cs >= 64) {
+        g.cs = cs;
+        break;
+      }
+  }
   // PDS_GEMM_CTAS caps the CTAs of every GEMM (a tuning knob; default: one per SM).
   static const int env_cap = [] {
     const char* v = std::getenv("PDS_GEMM_CTAS");
@@ -1161,14 +1238,14 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   g.grid = g.groups * gs;
 }
 
-template <int BN, int EPI>
-pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t st,
-                  std::string* err) {
-  using Cf = Cfg<BN>;
+template <int BN, int EPI, bool PAIR>
+pds_status launch_impl(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t st,
+                       std::string* err) {
+  using Cf = Cfg<BN, PAIR>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, EPI>,
+    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, EPI, PAIR>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(Cf::kSmem));
   });
@@ -1206,7 +1283,8 @@ pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t 
       cfg.attrs = attr;
       cfg.numAttrs = na;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, EPI>, &cfg) != cudaSuccess || n < 1) {
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, EPI, PAIR>, &cfg) != cudaSuccess ||
+          n < 1) {
         cudaGetLastError();
         n = 1;
       }
@@ -1226,12 +1304,21 @@ pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t 
   cfg.gridDim = dim3(g.grid);
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t ce = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, EPI>, maps, g);
+  cudaError_t ce = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, EPI, PAIR>, maps, g);
   if (ce != cudaSuccess) {
     *err = std::string("gemm launch: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;
   }
   return PDS_OK;
+}
+
+template <int BN, int EPI>
+pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t st,
+                  std::string* err) {
+  if constexpr (BN == 256) {
+    if (g.pair) return launch_impl<BN, EPI, true>(c, maps, g, st, err);
+  }
+  return launch_impl<BN, EPI, false>(c, maps, g, st, err);
 }
 
 }  // namespace
@@ -1410,7 +1497,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   g.wrows0 = N;
   g.c_out = Cout;
   g.ldc = N;
-  make_schedule(g, c, M, N / kNoAllocBN, K, kNoAllocBN, grid_cap);
+  make_schedule(g, c, M, N / kNoAllocBN, K, kNoAllocBN, grid_cap, false);
   g.cs = 1;  // a plain launch, without clusters
   GemmMaps maps{};
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
@@ -1422,11 +1509,11 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   g.partials = partials;
   g.counters = counters;
 
-  using Cf = Cfg<kNoAllocBN>;
+  using Cf = Cfg<kNoAllocBN, false>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<kNoAllocBN, kEpiPlain>,
+    attr_err = cudaFuncSetAttribute(gemm_kernel<kNoAllocBN, kEpiPlain, false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(Cf::kSmem));
   });
@@ -1439,7 +1526,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cf::kSmem;
   cfg.stream = st;
-  ce = cudaLaunchKernelEx(&cfg, gemm_kernel<kNoAllocBN, kEpiPlain>, maps, g);
+  ce = cudaLaunchKernelEx(&cfg, gemm_kernel<kNoAllocBN, kEpiPlain, false>, maps, g);
   if (ce != cudaSuccess) {
     *err = std::string("gemm launch: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;
