@@ -86,6 +86,10 @@ struct GemmArgs {
   // with cta_group::2 MMAs, each loading its own 128 rows of A and half of
   // the BN weight rows (no multicast).
   int pair;
+  // Cluster split-K (residual GEMMs in pair mode): each cluster of 2*split
+  // CTAs computes one 256 x BN tile, pair q over the q-th of `split` equal
+  // k ranges, and finishes it through distributed shared memory.  0: off.
+  int split;
   int wrows0, wrows1;  // rows of weight blocks 0 and 1 (concatenated along N)
   int pair_mode;       // W tile = 128 rows of block 0 then the same rows of block 1
   uint32_t* status;
@@ -109,7 +113,7 @@ struct Cfg {
   static constexpr uint32_t kBBytes = kBRows * BK * 2;
   static constexpr uint32_t kStage = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
-  static constexpr int kBars = 2 * kStages + 5 + 4;
+  static constexpr int kBars = 2 * kStages + 5 + 4 + 2;
   // The last tile's residual epilogue reuses the drained stages: 16 KB boxes,
   // BN/32 float32 residual boxes (32 columns x 128 rows) then BN/64 bf16 boxes
   // of the next GEMM's operand (64 columns x 128 rows).
@@ -592,25 +596,25 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
   }
 }
 
-// Residual epilogue of a CTA's last tile, through shared memory.  The
-// producer has loaded the residual tile into the drained stages (one barrier
-// per stage).  Each thread adds its row's accumulator (TMEM; a split tile
-// has been finished there first) to the residual in place (h), writes
+// Residual epilogue of a CTA's last tile, through shared memory, for this
+// thread's 32-column chunks jbeg .. jbeg + jcnt - 1 (jbeg even).  The
+// producer has loaded the residual boxes of chunks box_base .. into the
+// drained stages (box j - box_base, one barrier per stage).  Each thread
+// takes its row's accumulator from acc(j, v) (TMEM, or TMEM plus the other
+// split contributors' slices), adds it to the residual in place (h), writes
 // bf16(h * gain) to its warp's staging area and sums h^2 per 64 columns;
 // each warp then stores its 32 rows of each box with TMA.  No global load
-// or store of a tile element goes through registers.  Returns false if a
-// wait gave up.
-template <int BN, bool PAIR>
+// or store of a tile element goes through registers.  The threads of a
+// column half (ch) call it together.  Returns false if a wait gave up.
+template <int BN, bool PAIR, typename Acc>
 __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const GemmMaps& maps,
-                                                    uint32_t taddr, int mt, int nt, int row,
-                                                    int ch, int lane, uint32_t sbase, int n_it,
-                                                    uint32_t bar_res0, volatile int* abort_flag,
-                                                    const Stage& st, float* gain_sm) {
+                                                    int mt, int nt, int row, int ch, int lane,
+                                                    uint32_t sbase, int n_it, uint32_t bar_res0,
+                                                    volatile int* abort_flag, const Stage& st,
+                                                    float* gain_sm, int jbeg, int jcnt,
+                                                    int box_base, Acc&& acc) {
   using namespace sm100;
   using C = Cfg<BN, PAIR>;
-  constexpr int EPI = kEpiResid;  // for the trace hook
-  (void)EPI;
-  constexpr int kChunks = BN / 64;  // 32-column chunks of this thread's half
   const ResidEpilogue& e = g.resid;
   const int lane_grp = row >> 5;
   const int m = mt * BM + row;
@@ -619,24 +623,24 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
   const uint64_t pol_keep = policy_evict_last();
   const uint32_t sw = static_cast<uint32_t>(row & 7);
   const uint32_t a_stage = smem_u32(st.base);  // this warp's 32 rows x 64 bf16 of the operand
-  // The gain of this half's columns, once, by the half's first warp.
+  // The gain of this thread's columns, once, by the half's first warp.
   if (e.gain) {
-    if (lane_grp == 0 && lane < BN / 8)
+    if (lane_grp == 0 && lane < jcnt * 8)
       reinterpret_cast<float4*>(gain_sm)[ch * (BN / 8) + lane] =
-          __ldg(reinterpret_cast<const float4*>(e.gain + nt * BN + ch * (BN / 2)) + lane);
+          __ldg(reinterpret_cast<const float4*>(e.gain + nt * BN + jbeg * 32) + lane);
     named_bar_sync(2 + ch, 128);
   }
   const float4* gs = reinterpret_cast<const float4*>(gain_sm) + ch * (BN / 8);
   float ss = 0.f;
 #pragma unroll 1
-  for (int c = 0; c < kChunks; ++c) {
-    const int j = ch * kChunks + c;  // 32-column chunk = residual box j
+  for (int c = 0; c < jcnt; ++c) {
+    const int j = jbeg + c;  // 32-column chunk
+    const int b = j - box_base;  // its residual box
     const int n0 = nt * BN + j * 32;
-    if (!mbar_wait(bar_res0 + 8u * (j / C::kBoxesPerStage), 0, abort_flag, g.status)) return false;
-    if (c == 0 && row == 0 && ch == 0) PDS_GEMM_TRACE_HOOK(blockIdx.x, 7);
+    if (!mbar_wait(bar_res0 + 8u * (b / C::kBoxesPerStage), 0, abort_flag, g.status)) return false;
     float v[32];
-    tmem_load32(taddr + j * 32, v);
-    const uint32_t rrow = epi_box<BN, PAIR>(sbase, n_it, j) + static_cast<uint32_t>(row) * 128u;
+    acc(j, v);
+    const uint32_t rrow = epi_box<BN, PAIR>(sbase, n_it, b) + static_cast<uint32_t>(row) * 128u;
     if (e.gain && (c & 1) == 0 && c > 0) {
       // the previous pair's operand store has read the staging area
       if (lane == 0) bulk_wait_read_all();
@@ -671,7 +675,8 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && warp_live)
-      tma_store_2d(&maps.e[1], epi_box<BN, PAIR>(sbase, n_it, j) + lane_grp * 4096u, n0, m0w, pol_keep);
+      tma_store_2d(&maps.e[1], epi_box<BN, PAIR>(sbase, n_it, b) + lane_grp * 4096u, n0, m0w,
+                   pol_keep);
     if (e.gain && (j & 1)) {
       if (lane == 0 && warp_live) {
         tma_store_2d(&maps.e[2], a_stage, n0 - 32, m0w, pol_keep);
@@ -687,6 +692,135 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
   }
   __syncwarp();
   return true;
+}
+
+// Cluster split-K of a residual GEMM: the cluster's S pairs compute one
+// 256 x BN tile over S consecutive k ranges.  The tile's eight 32-column
+// chunks are dealt to the pairs in 64-column units (pair q finishes chunks
+// [first, first + count)); every CTA sends the chunks it does not finish
+// to the CTA of the same rank in the finishing pair, straight into that
+// CTA's drained stages (after its residual boxes), and finishes its own.
+struct SplitSlice {
+  int first, count;
+};
+__host__ __device__ __forceinline__ SplitSlice split_slice(int S, int q) {
+  const int base = 4 / S, extra = 4 % S;
+  const int units = base + (q < extra ? 1 : 0);
+  const int first = q * base + (q < extra ? q : extra);
+  return SplitSlice{2 * first, 2 * units};
+}
+__device__ __forceinline__ int split_owner(int S, int j) {
+  for (int q = 0; q < S - 1; ++q) {
+    const SplitSlice sl = split_slice(S, q);
+    if (j < sl.first + sl.count) return q;
+  }
+  return S - 1;
+}
+// Box of the finishing CTA (pair q, slice sl) that receives chunk j from pair p.
+__device__ __forceinline__ int split_recv_box(int S, int q, const SplitSlice& sl, int j, int p) {
+  return sl.count + (j - sl.first) * (S - 1) + (p < q ? p : p - 1);
+}
+
+// The split epilogue of one CTA (pair p of the cluster, rank r in the
+// pair).  Returns false if a wait gave up.
+template <int BN>
+__device__ __forceinline__ bool split_resid_epilogue(
+    const GemmArgs& g, const GemmMaps& maps, uint32_t taddr, int mt, int nt, int row, int ch,
+    int lane, uint32_t sbase, int grp, uint32_t bar_res0, uint32_t bar_ready, uint32_t bar_recv,
+    volatile int* abort_flag, const Stage& st, float* gain_sm, uint32_t crank, bool leader) {
+  using namespace sm100;
+  static_assert(BN == 256, "eight 32-column chunks in four 64-column units");
+  constexpr bool PAIR = true;
+  const int S = g.split;
+  const int p = static_cast<int>(crank >> 1), r = static_cast<int>(crank & 1u);
+  const int grp0 = grp - p;  // the cluster's first group
+  auto n_it_of = [&](int q) { return seg_begin(g, grp0 + q + 1) - seg_begin(g, grp0 + q); };
+  const SplitSlice mine = split_slice(S, p);
+  const int my_n_it = n_it_of(p);
+  // 1. receive: expect the other pairs' slices, then tell them our stages
+  //    are free (every MMA of this pair has completed: the accumulator is full)
+  if (leader) {
+    mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(mine.count * (S - 1)) * 16384u);
+    for (int q = 0; q < S; ++q)
+      if (q != p) mbar_arrive_cluster(mapa_shared(bar_ready, static_cast<uint32_t>(2 * q + r)));
+  }
+  // 2. send: this half's share of the chunks other pairs finish.  With room
+  //    in the drained stages after the received slices, a chunk is staged
+  //    there and each warp bulk-copies its 32 rows (4 KB); otherwise the
+  //    rows go out as 16-byte asynchronous remote stores.
+  if (!mbar_wait(bar_ready, 0, abort_flag, g.status)) return false;
+  tc_fence_after();
+  {
+    const int out_box0 = mine.count * S;  // first free box of the drained stages
+    const bool bulk = out_box0 + (BN / 32 - mine.count) <= Cfg<BN, PAIR>::kStages * 2;
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
+    const uint32_t wrow0 = static_cast<uint32_t>(row & ~31) * 128u;  // this warp's 32 rows
+    int k = 0;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      if (j >= mine.first && j < mine.first + mine.count) continue;
+      const int kk = k++;
+      if ((kk & 1) != ch) continue;
+      const int q = split_owner(S, j);
+      const SplitSlice sl = split_slice(S, q);
+      const uint32_t dst_rank = static_cast<uint32_t>(2 * q + r);
+      const uint32_t dst_box = epi_box<BN, PAIR>(sbase, n_it_of(q), split_recv_box(S, q, sl, j, p));
+      const uint32_t rbar = mapa_shared(bar_recv, dst_rank);
+      float v[32];
+      tmem_load32(taddr + j * 32, v);
+      if (bulk) {
+        const uint32_t src_box = epi_box<BN, PAIR>(sbase, my_n_it, out_box0 + kk);
+        const uint32_t src = src_box + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          st_shared_f4(src + ((static_cast<uint32_t>(q4) ^ sw) << 4),
+                       make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          bulk_copy_to_cluster(mapa_shared(dst_box + wrow0, dst_rank), src_box + wrow0, 4096u,
+                               rbar);
+      } else {
+        const uint32_t dst = mapa_shared(dst_box + static_cast<uint32_t>(row) * 128u, dst_rank);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          st_async_f4(dst + ((static_cast<uint32_t>(q4) ^ sw) << 4),
+                      make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]), rbar);
+      }
+    }
+  }
+  // 3. finish this pair's chunks: the contributors in k order (pair order)
+  if (!mbar_wait(bar_recv, 0, abort_flag, g.status)) return false;
+  auto acc = [&](int j, float (&v)[32]) {
+    float own[32];
+    tmem_load32(taddr + j * 32, own);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
+    for (int q = 0; q < S; ++q) {
+      if (q == p) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += own[i];
+      } else {
+        const uint32_t src = epi_box<BN, PAIR>(sbase, my_n_it, split_recv_box(S, p, mine, j, q)) +
+                             static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 x = ld_shared_f4(src + ((static_cast<uint32_t>(q4) ^ sw) << 4));
+          v[4 * q4] += x.x;
+          v[4 * q4 + 1] += x.y;
+          v[4 * q4 + 2] += x.z;
+          v[4 * q4 + 3] += x.w;
+        }
+      }
+    }
+  };
+  // halves: two 64-column units each, or the first half alone for one unit
+  const int half_cnt = mine.count >= 4 ? mine.count / 2 : (ch == 0 ? mine.count : 0);
+  const int jbeg = mine.first + (mine.count >= 4 ? ch * (mine.count / 2) : 0);
+  if (half_cnt == 0) return true;
+  return resid_epilogue_smem<BN, PAIR>(g, maps, mt, nt, row, ch, lane, sbase, my_n_it, bar_res0,
+                                       abort_flag, st, gain_sm, jbeg, half_cnt, mine.first, acc);
 }
 
 template <int BN, int EPI, bool PAIR>
@@ -711,6 +845,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_tempty = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t bar_drain = bar0 + 8u * (2 * S + 4);
   const uint32_t bar_res0 = bar0 + 8u * (2 * S + 5);  // residual boxes landed, one per stage
+  const uint32_t bar_ready = bar0 + 8u * (2 * S + 9);  // split: the other pairs may send
+  const uint32_t bar_recv = bar0 + 8u * (2 * S + 10);  // split: their slices have landed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -729,6 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_drain, 1);
     for (int f = 0; f < 4; ++f) mbar_init(bar_res0 + 8u * f, 1);
+    mbar_init(bar_ready, g.split > 1 ? g.split - 1 : 1);
+    mbar_init(bar_recv, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -759,9 +897,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (g.cs > 1) cluster_sync();
   const uint32_t tmem_base = misc[0];
   const uint16_t cmask = static_cast<uint16_t>((1u << g.cs) - 1);
-  // A pair: rank 0 issues the MMAs and owns the stage-full and
-  // accumulator-empty barriers both CTAs' copies and epilogues signal.
-  const uint32_t prank = PAIR ? cluster_rank() : 0u;
+  // A pair (cluster ranks 2k, 2k+1): the even CTA issues the MMAs and owns
+  // the stage-full and accumulator-empty barriers both CTAs' copies and
+  // epilogues signal.
+  const uint32_t crank = g.cs > 1 ? cluster_rank() : 0u;
+  const uint32_t prank = PAIR ? (crank & 1u) : 0u;
+  const uint32_t lead = crank & ~1u;  // the pair leader's cluster rank
+  const uint16_t pmask = static_cast<uint16_t>(3u << lead);
   if (threadIdx.x == 0) PDS_GEMM_TRACE_HOOK(cta, 0);
 
   // Everything above overlaps the previous kernel when launched with
@@ -792,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slice = BN / g.cs;  // weight rows this CTA loads for the cluster
       const int r0 = (g.cs > 1 && !PAIR ? static_cast<int>(cluster_rank()) : 0) * slice;
       // where a stage's copies complete: the pair leader's barrier, or our own
-      auto full_bar = [&](int s) { return PAIR ? mapa_shared(bar_full(s), 0) : bar_full(s); };
+      auto full_bar = [&](int s) { return PAIR ? mapa_shared(bar_full(s), lead) : bar_full(s); };
       auto load_w = [&](int s, int nt, int kb) {
         if constexpr (PAIR) {
           // this CTA's half of the pair's BN weight rows
@@ -864,16 +1006,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile's residual is loaded too: this CTA may be the one to finish it.
       if (EPI == kEpiResid && ok && it1 > it0) {
         const uint64_t pol_r = policy_evict_first();  // the residual's last read
+        // the whole tile's boxes, or the slice this CTA finishes in a split
+        int rfirst = 0, rcount = C::kResBoxes;
+        if (g.split > 1) {
+          const SplitSlice sl = split_slice(g.split, static_cast<int>(crank >> 1));
+          rfirst = sl.first;
+          rcount = sl.count;
+        }
+        const int rstages = (rcount + C::kBoxesPerStage - 1) / C::kBoxesPerStage;
         int issued_res = 0;
-        for (int f = 0; f < C::kResStages; ++f) {
+        for (int f = 0; f < rstages; ++f) {
           const int v = issued + f;
           const int s = v % S;
           if (v >= S && !mbar_wait(bar_empty(s), ((v / S) & 1) ^ 1, abort_flag, g.status)) break;
-          const int nb = min(C::kBoxesPerStage, C::kResBoxes - f * C::kBoxesPerStage);
+          const int nb = min(C::kBoxesPerStage, rcount - f * C::kBoxesPerStage);
           mbar_arrive_expect_tx(bar_res0 + 8u * f, static_cast<uint32_t>(nb) * 16384u);
           for (int b = 0; b < nb; ++b)
             tma_load_2d(sbase + s * C::kStage + b * 16384u, &maps.e[0], bar_res0 + 8u * f,
-                        nt * BN + (f * C::kBoxesPerStage + b) * 32, mt * BM, pol_r);
+                        nt * BN + (rfirst + f * C::kBoxesPerStage + b) * 32, mt * BM, pol_r);
           ++issued_res;
         }
         // none of these copies may still be landing when the CTA exits,
@@ -913,7 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if constexpr (PAIR) {
-            umma_commit_pair_mc(bar_empty(s), 0x3);  // the stage is free in both CTAs
+            umma_commit_pair_mc(bar_empty(s), pmask);  // the stage is free in both CTAs
           } else if (g.cs > 1) {
             umma_commit_mc(bar_empty(s), cmask);  // the stage is free in every CTA's view
           } else {
@@ -923,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if constexpr (PAIR) {
-          umma_commit_pair_mc(bar_tfull(ab), 0x3);  // both halves of the accumulator
+          umma_commit_pair_mc(bar_tfull(ab), pmask);  // both halves of the accumulator
         } else {
           umma_commit(bar_tfull(ab));
         }
@@ -968,6 +1118,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = mt + nt * g.tiles_m;
       Fixup fx{false, 0, 0, grp, rank, unit};
       bool run = true;
+      if constexpr (EPI == kEpiResid && PAIR) {
+        if (g.split > 1) {
+          // the CTA's only tile, finished with the cluster's other pairs
+          const bool ok = split_resid_epilogue<BN>(
+              g, maps, taddr, mt, nt, row, ch, lane, sbase, grp, bar_res0, bar_ready, bar_recv,
+              abort_flag, st, reinterpret_cast<float*>(smem + S * C::kStage + 1024), crank, leader);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_tempty(ab), lead));
+          if (!ok) break;
+          ++sg;
+          continue;
+        }
+      }
       if (!(k0 == 0 && k1 == g.kb)) {
         const int slot = (it0 / g.kb == unit) ? 0 : 1;
         float4* mine = reinterpret_cast<float4*>(g.partials) +
@@ -1014,9 +1178,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           fx.active = false;
         }
         if (EPI == kEpiResid && last) {
-          if (!resid_epilogue_smem<BN, PAIR>(g, maps, taddr, mt, nt, row, ch, lane, sbase, it1 - it0,
-                                       bar_res0, abort_flag, st,
-                                       reinterpret_cast<float*>(smem + S * C::kStage + 1024)))
+          auto acc = [&](int j, float (&v)[32]) { tmem_load32(taddr + j * 32, v); };
+          if (!resid_epilogue_smem<BN, PAIR>(g, maps, mt, nt, row, ch, lane, sbase, it1 - it0,
+                                             bar_res0, abort_flag, st,
+                                             reinterpret_cast<float*>(smem + S * C::kStage + 1024),
+                                             ch * (BN / 64), BN / 64, 0, acc))
             break;
         } else {
           run_epilogue<BN, EPI>(g, taddr, mt, nt, row, ch, lane, rscale, st);
@@ -1030,7 +1196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         if (PAIR && prank != 0) {
-          mbar_arrive_cluster(mapa_shared(bar_tempty(ab), 0));
+          mbar_arrive_cluster(mapa_shared(bar_tempty(ab), lead));
         } else {
           mbar_arrive(bar_tempty(ab));
         }
@@ -1157,7 +1323,7 @@ uint32_t weight_box_rows(const GemmArgs& g, int bn) {
 }
 
 void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, int bn,
-                   int max_grid = kGemmMaxGrid, bool allow_pair = true) {
+                   int max_grid = kGemmMaxGrid, bool allow_pair = true, int split = 0) {
   g.M = M;
   g.K = K;
   g.tiles_m = (M + BM - 1) / BM;
@@ -1185,6 +1351,33 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   }();
   g.cs = 1;
   g.pair = 0;
+  g.split = 0;
+  if (env_pair && bn == 256 && gs % 2 == 0 && allow_pair && split != 0) {
+    // Cluster split-K (residual epilogues only; split = 0 elsewhere): one
+    // cluster of 2S CTAs per 256-row pair tile when the pair tiles alone
+    // would leave at least half of the SMs idle.  split < 0 picks the
+    // largest S (at most 4) whose CTAs fit one per SM; split > 0 caps it.
+    const int ctas = std::min({c.num_sms > 0 ? c.num_sms : 148, kGemmMaxGrid, max_grid});
+    const int units = (g.tiles_m / 2) * tiles_n;
+    int S = 1;
+    for (int t = 4; t >= 2; --t)
+      if (2 * t * units <= ctas && t <= g.kb && (split < 0 || t <= split)) {
+        S = t;
+        break;
+      }
+    if (S >= 2) {
+      g.gs = 2;
+      g.mgs = g.tiles_m / 2;
+      g.units = units;
+      g.total = units * g.kb;
+      g.groups = S * units;
+      g.grid = 2 * g.groups;
+      g.pair = 1;
+      g.cs = 2 * S;
+      g.split = S;
+      return;
+    }
+  }
   if (env_pair && bn == 256 && gs % 2 == 0 && allow_pair) {
     g.pair = 1;
     g.cs = 2;
@@ -1269,31 +1462,59 @@ pds_status launch_impl(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStre
   cudaLaunchAttribute attr[2];
   int na = 0;
   if (g.cs > 1) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = g.cs;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
     // never more clusters than fit on the GPU at once (one CTA per SM)
     static std::mutex mu;
-    static int max_clusters[5] = {0, 0, 0, 0, 0};
-    std::lock_guard<std::mutex> lock(mu);
-    if (!max_clusters[g.cs]) {
-      cfg.gridDim = dim3(g.cs);
-      cfg.attrs = attr;
-      cfg.numAttrs = na;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, EPI, PAIR>, &cfg) != cudaSuccess ||
-          n < 1) {
-        cudaGetLastError();
-        n = 1;
+    static int max_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    auto fit = [&](int cs) {
+      std::lock_guard<std::mutex> lock(mu);
+      if (!max_clusters[cs]) {
+        cudaLaunchAttribute ca[1];
+        ca[0].id = cudaLaunchAttributeClusterDimension;
+        ca[0].val.clusterDim.x = cs;
+        ca[0].val.clusterDim.y = 1;
+        ca[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3(cs);
+        q.attrs = ca;
+        q.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, EPI, PAIR>, &q) != cudaSuccess ||
+            n < 1) {
+          cudaGetLastError();
+          n = 1;
+        }
+        max_clusters[cs] = n;
       }
-      max_clusters[g.cs] = n;
+      return max_clusters[cs];
+    };
+    if (g.split > 1) {
+      // all of a split GEMM's clusters at once, or fewer pairs per tile
+      int S = g.split;
+      while (S >= 2 && fit(2 * S) < g.units) --S;
+      if (S != g.split) {
+        if (S >= 2) {
+          g.split = S;
+          g.cs = 2 * S;
+          g.groups = S * g.units;
+          g.grid = 2 * g.groups;
+        } else {
+          make_schedule(g, c, g.M, g.tiles_n, g.K, BN, kGemmMaxGrid, true, 0);
+        }
+      }
     }
-    const int cap_groups = std::max(1, max_clusters[g.cs] * g.cs / g.gs);
-    if (g.groups > cap_groups) {
-      g.groups = cap_groups;
-      g.grid = g.groups * g.gs;
+    if (g.cs > 1 && g.split < 2) {
+      const int cap_groups = std::max(1, fit(g.cs) * g.cs / g.gs);
+      if (g.groups > cap_groups) {
+        g.groups = cap_groups;
+        g.grid = g.groups * g.gs;
+      }
+    }
+    if (g.cs > 1) {
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = g.cs;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      ++na;
     }
   }
   if (c.pdl) {
@@ -1350,6 +1571,12 @@ pds_status tc_gemm_plain(TcContext& c, const uint16_t* A, const uint16_t* W, flo
 
 pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int M, int N, int K,
                          const ResidEpilogue& e, cudaStream_t st, std::string* err) {
+  // PDS_GEMM_SPLIT caps the pairs of the cluster split-K (0 turns it off; a
+  // tuning knob).
+  static const int env_split = [] {
+    const char* v = std::getenv("PDS_GEMM_SPLIT");
+    return v ? std::atoi(v) : -1;
+  }();
   // PDS_GEMM_BN_RESID=128 forces 128-wide tiles (a tuning knob).
   static const int env_bn = [] {
     const char* v = std::getenv("PDS_GEMM_BN_RESID");
@@ -1360,7 +1587,7 @@ pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int
   g.wrows0 = N;
   g.resid = e;
   g.resid_n = N;
-  make_schedule(g, c, M, N / bn, K, bn);
+  make_schedule(g, c, M, N / bn, K, bn, kGemmMaxGrid, true, env_split);
   GemmMaps maps{};
   pds_status rc;
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;

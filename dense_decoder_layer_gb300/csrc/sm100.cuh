@@ -167,6 +167,29 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                : "memory");
 }
 
+// Asynchronous store of 16 bytes to another CTA's shared memory (cluster
+// window address), completing as a byte-count transaction on an mbarrier of
+// that CTA (cluster window address).
+__device__ __forceinline__ void st_async_f4(uint32_t cluster_addr, float4 v, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          cluster_addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_bar)
+      : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// another CTA's (cluster window address), completing as a byte-count
+// transaction on an mbarrier of the destination CTA.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
+                                                     uint32_t bytes, uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_cluster),
+      "r"(src), "r"(bytes), "r"(cluster_bar)
+      : "memory");
+}
+
 // CTA-pair load: one box into this CTA's shared memory, completing on an
 // mbarrier given by its cluster-window address, which may be in the peer
 // CTA of the pair (the one that issues the pair's MMAs).
