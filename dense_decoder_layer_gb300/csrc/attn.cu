@@ -298,9 +298,9 @@ cudaError_t launch_flash(const uint16_t* q, const uint16_t* k, const uint16_t* v
 
 }  // namespace
 
-pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                        uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
-                        std::string* err) {
+pds_status tc_attention_mma(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            uint16_t* o, int B, int start_pos, int H, int Hkv, int hd,
+                            cudaStream_t st, std::string* err) {
   cudaError_t ce = hd == 128 ? launch_flash<128>(q, k, v, o, B, start_pos, H, Hkv, c.pdl, st)
                              : launch_flash<64>(q, k, v, o, B, start_pos, H, Hkv, c.pdl, st);
   if (ce != cudaSuccess) {

@@ -1,0 +1,458 @@
+// GQA causal attention of the new rows over the cache prefix plus the new
+// rows, on the tcgen05 tensor cores (frink-models 0.29.0
+// src/decoder/cuda_prefill.rs, PrefillParams: prefix_k / prefix_v are the
+// cache's first start_pos rows; attn_scale = 1/sqrt(head_dim); no softcap,
+// no window).  Query row b sits at position start_pos + b and reads kv head
+// h / (H / Hkv).
+//
+// One CTA per (query head, 128 query rows), heaviest row tiles first.
+//   warp 0      TMA producer: the Q tile once, then K and V tiles of 128
+//               keys (128-byte swizzle) into two-stage rings, K one ahead
+//   warp 1      tcgen05.mma issuer: S_j = Q K_j^T into one of two TMEM
+//               buffers, O += P_j V_j into a TMEM accumulator (V read
+//               MN-major straight from its cache layout)
+//   warps 4-19  softmax, four threads per query row (TMEM lane), each with
+//               32 of the tile's keys: S_j from TMEM, causal mask, the row
+//               maximum (the quarters exchange theirs through shared
+//               memory), exp2 of the scaled score against the row's
+//               reference maximum, P_j as bf16 into shared memory (the A
+//               operand of the P.V MMA).  The reference maximum moves only
+//               when a row's maximum grows by more than 2^8 (the O row in
+//               TMEM is then rescaled once), so exp2 values stay <= 256.  At
+//               the end the quarters add their row sums in order and each
+//               divides and stores a quarter of the O row.
+// S_{j+1} is computed while the softmax works on S_j.  Every wait is
+// bounded; a wait that gives up sets the status word and the CTA exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tc.h"
+
+namespace pds {
+namespace {
+
+constexpr int kRows = 128;  // query rows per CTA
+constexpr int kKeys = 128;  // keys per tile
+constexpr int kRowSplit = 4;  // softmax threads per query row
+constexpr int kSoftmaxFirstWarp = 4;
+constexpr int kSoftmaxThreads = 128 * kRowSplit;
+constexpr int kAttnThreads = 32 * kSoftmaxFirstWarp + kSoftmaxThreads;
+constexpr float kRescaleLog2 = 8.0f;  // move the reference max beyond a 2^8 growth
+
+template <int HD>
+struct AttnCfg {
+  static constexpr uint32_t kTile = 128u * HD * 2u;  // Q, K or V tile (bf16)
+  static constexpr uint32_t kP = 128u * kKeys * 2u;  // P tile (bf16)
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK0 = kTile;             // K stage s at kK0 + s kTile
+  static constexpr uint32_t kV0 = kK0 + 2u * kTile;  // V stage s at kV0 + s kTile
+  static constexpr uint32_t kP0 = kV0 + 2u * kTile;  // one P buffer
+  static constexpr uint32_t kX = kP0 + kP;           // row maxima / sums of the halves
+  static constexpr uint32_t kBar = kX + 2u * kRowSplit * 128u * 4u;
+  static constexpr int kNumBars = 16;
+  static constexpr size_t kSmem = 1024 + kBar + kNumBars * 8 + 16;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+  // TMEM: S buffers at columns 0 and 128, O at 256
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct AttnMaps {
+  CUtensorMap q, k, v;
+};
+struct AttnArgs {
+  uint16_t* o;
+  int B, s, H, Hkv;
+  float scale_log2;
+  uint32_t* status;
+};
+
+// K-major SW128 descriptor of a 128-row operand whose K extent is split in
+// 64-element (128-byte) column blocks of 16 KB each.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kstep) {
+  // k-step of 16 elements: 32 bytes inside a 128-byte block, 4 per block
+  return sm100::smem_desc_sw128(base + static_cast<uint32_t>(kstep >> 2) * 16384u +
+                                static_cast<uint32_t>(kstep & 3) * 32u);
+}
+
+// MN-major SW128 descriptor of the V tile [128 keys][HD] as the B operand
+// (N = HD, K = keys) of O += P V: rows are keys (128 bytes of 64 head
+// channels each, 8-row groups 1024 bytes apart: the stride byte offset),
+// head channels 64..127 are the next 16 KB block (the leading byte offset).
+__device__ __forceinline__ uint64_t v_desc(uint32_t base, int kstep) {
+  const uint32_t a = base + static_cast<uint32_t>(kstep) * 16u * 128u;  // 16 key rows
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((a >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(16384u >> 4) << 16;  // leading byte offset: next 64 channels
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;   // stride byte offset: next 8 keys
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// 2^x on the special-function unit (approximate, subnormal results flushed).
+__device__ __forceinline__ float exp2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Pairwise (tree) maximum and sum of n values.
+template <int N>
+__device__ __forceinline__ float tree_max(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else {
+    return fmaxf(tree_max<N / 2>(v), tree_max<N / 2>(v + N / 2));
+  }
+}
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else {
+    return tree_sum<N / 2>(v) + tree_sum<N / 2>(v + N / 2);
+  }
+}
+
+// kind::f16 instruction descriptor: bf16 x bf16 -> f32, M x N, B MN-major if b_mn.
+__host__ __device__ constexpr uint32_t idesc_attn(int M, int N, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_tc_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ AttnArgs a) {
+  using namespace sm100;
+  using C = AttnCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const uint32_t bar0 = sbase + C::kBar;
+  const uint32_t bar_q = bar0;
+  auto bar_k_full = [&](int st) { return bar0 + 8u * (1 + st); };
+  auto bar_k_empty = [&](int st) { return bar0 + 8u * (3 + st); };
+  auto bar_v_full = [&](int st) { return bar0 + 8u * (5 + st); };
+  auto bar_v_empty = [&](int st) { return bar0 + 8u * (7 + st); };
+  auto bar_s_full = [&](int b) { return bar0 + 8u * (9 + b); };
+  auto bar_s_free = [&](int b) { return bar0 + 8u * (11 + b); };
+  const uint32_t bar_p_full = bar0 + 8u * 13;  // phase j: P_j is in shared memory
+  const uint32_t bar_pv = bar0 + 8u * 14;      // phase j: O += P_j V_j has completed
+  const uint32_t bar_drain = bar0 + 8u * 15;   // every MMA of the CTA has completed
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kBar + C::kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = gridDim.y - 1 - blockIdx.y;  // longest row tiles first
+  const int h = blockIdx.x, g = h / (a.H / a.Hkv);
+  const int b0 = qt * kRows;
+  const int last_row = min(b0 + kRows, a.B) - 1;
+  const int nkt = (a.s + last_row + 1 + kKeys - 1) / kKeys;  // key tiles this CTA reads
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_k_full(i), 1);
+      mbar_init(bar_k_empty(i), 1);
+      mbar_init(bar_v_full(i), 1);
+      mbar_init(bar_v_empty(i), 1);
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_s_free(i), kSoftmaxThreads / 32);  // one arrival per softmax warp
+    }
+    mbar_init(bar_p_full, kSoftmaxThreads / 32);
+    mbar_init(bar_pv, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&maps.q);
+    tma_prefetch_map(&maps.k);
+    tma_prefetch_map(&maps.v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  grid_dep_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // q, k and v are the previous kernel's output
+      grid_dep_wait();
+      const uint64_t pol = policy_evict_normal();
+      mbar_arrive_expect_tx(bar_q, C::kTile);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_2d(sbase + C::kQ + c * 16384u, &maps.q, bar_q, h * HD + c * 64, b0, pol);
+      // K_j is freed by S_j, V_j by O += P_j V_j, which comes later: K
+      // runs one tile ahead of V (K_0, K_1, V_0, K_2, V_1, ...)
+      auto load = [&](const CUtensorMap* map, uint32_t base, uint32_t full, uint32_t empty, int j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(empty + 8u * st, ((j >> 1) - 1) & 1, abort_flag, a.status))
+          return false;
+        mbar_arrive_expect_tx(full + 8u * st, C::kTile);
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_2d(base + st * C::kTile + c * 16384u, map, full + 8u * st, g * HD + c * 64,
+                      j * kKeys, pol);
+        return true;
+      };
+      bool ok = load(&maps.k, sbase + C::kK0, bar_k_full(0), bar_k_empty(0), 0);
+      for (int j = 0; ok && j < nkt; ++j) {
+        if (j + 1 < nkt && !(ok = load(&maps.k, sbase + C::kK0, bar_k_full(0), bar_k_empty(0), j + 1)))
+          break;
+        ok = load(&maps.v, sbase + C::kV0, bar_v_full(0), bar_v_empty(0), j);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_attn(128, kKeys, false);
+      constexpr uint32_t kIdPV = idesc_attn(128, HD, true);
+      const uint32_t tm_o = tmem + 256;
+      bool ok = mbar_wait(bar_q, 0, abort_flag, a.status);
+      auto issue_s = [&](int j) {
+        const int st = j & 1;
+        if (!mbar_wait(bar_k_full(st), (j >> 1) & 1, abort_flag, a.status)) return false;
+        if (j >= 2 && !mbar_wait(bar_s_free(st), ((j >> 1) - 1) & 1, abort_flag, a.status))
+          return false;
+        tc_fence_after();
+        const uint32_t kb = sbase + C::kK0 + st * C::kTile;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          umma_bf16(tmem + st * 128u, kmajor_desc(sbase + C::kQ, k), kmajor_desc(kb, k), kIdS,
+                    k > 0 ? 1u : 0u);
+        umma_commit(bar_s_full(st));
+        umma_commit(bar_k_empty(st));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < nkt; ++j) {
+        if (j + 1 < nkt && !(ok = issue_s(j + 1))) break;
+        const int st = j & 1;
+        if (!(ok = mbar_wait(bar_v_full(st), (j >> 1) & 1, abort_flag, a.status))) break;
+        if (!(ok = mbar_wait(bar_p_full, j & 1, abort_flag, a.status))) break;
+        tc_fence_after();
+        const uint32_t pb = sbase + C::kP0;
+        const uint32_t vb = sbase + C::kV0 + st * C::kTile;
+#pragma unroll
+        for (int k = 0; k < kKeys / 16; ++k)
+          umma_bf16(tm_o, kmajor_desc(pb, k), v_desc(vb, k), kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit(bar_v_empty(st));
+        umma_commit(bar_pv);
+      }
+      umma_commit(bar_drain);
+      int dummy = 0;
+      mbar_wait(bar_drain, 0, &dummy, a.status);
+    }
+  } else if (warp >= kSoftmaxFirstWarp) {
+    const int sw_idx = warp - kSoftmaxFirstWarp;
+    const int part = sw_idx >> 2;                           // keys / O columns of this thread
+    const int r = (sw_idx & 3) * 32 + lane;                 // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float* xch = reinterpret_cast<float*>(smem + C::kX);   // [2 tiles][parts][128 rows]
+    const int pos = a.s + b0 + r;
+    constexpr int kPartKeys = kKeys / kRowSplit;
+    constexpr int kPartCols = HD / kRowSplit;
+    static_assert(kPartKeys % 32 == 0 && kPartCols % 16 == 0, "TMEM loads of the parts");
+    const float sc = a.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;  // m_ref in scaled (base-2) units
+    // Every softmax thread passes the named barriers of every tile, even
+    // after a wait has given up (ok false: the work is skipped), and a
+    // warp's threads agree on ok, so no barrier or warp-wide instruction is
+    // left waiting.
+    bool ok = true;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+      ok = ok && mbar_wait(bar, parity, abort_flag, a.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) tc_fence_after();
+    };
+    for (int j = 0; j < nkt; ++j) {
+      const int st = j & 1;
+      wait(bar_s_full(st), (j >> 1) & 1);
+      float sv[kPartKeys];
+      float mx = -INFINITY;  // raw score maximum (the scale is positive)
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < kPartKeys / 32; ++c) {
+          float t[32];
+          tmem_load32(tmem + lane_off + st * 128u + part * kPartKeys + c * 32, t);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sv[c * 32 + i] = t[i];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_s_free(st));
+        // causal mask and this part's maximum
+        const int key0 = j * kKeys + part * kPartKeys;
+        if (key0 + kPartKeys - 1 > a.s + b0) {  // some key past some row
+#pragma unroll
+          for (int i = 0; i < kPartKeys; ++i)
+            if (key0 + i > pos) sv[i] = -INFINITY;
+        }
+        mx = tree_max<kPartKeys>(sv);
+      }
+      // the row maximum: all parts
+      xch[(st * kRowSplit + part) * 128 + r] = mx;
+      named_bar_sync(1 + (warp & 3), 32 * kRowSplit);  // the warps of these 32 rows
+#pragma unroll
+      for (int q = 0; q < kRowSplit; ++q) mx = fmaxf(mx, xch[(st * kRowSplit + q) * 128 + r]);
+      if (!ok) continue;
+      const float mxs = mx * sc;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (j == 0) {
+        m_ref = mxs;  // key 0 is visible to every row: finite
+      } else if (mxs > m_ref + kRescaleLog2) {
+        alpha = exp2f(m_ref - mxs);
+        m_ref = mxs;
+        rescale = true;
+      }
+      // P = exp2(s * scale - m_ref) as bf16, and this part's row sum
+      uint32_t pk[kPartKeys / 2];
+#pragma unroll
+      for (int i = 0; i < kPartKeys / 2; ++i) {
+        sv[2 * i] = exp2_sfu(fmaf(sv[2 * i], sc, -m_ref));
+        sv[2 * i + 1] = exp2_sfu(fmaf(sv[2 * i + 1], sc, -m_ref));
+        pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+      }
+      const float sum = tree_sum<kPartKeys>(sv);
+      l = l * alpha + sum;
+      if (j > 0) {
+        // O += P_{j-1} V_{j-1} has completed: O is stable and the P buffer free
+        wait(bar_pv, (j - 1) & 1);
+        if (!ok) continue;
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c = 0; c < kPartCols / 16; ++c) {
+            float t[16];
+            const uint32_t ta = tmem + lane_off + 256u + part * kPartCols + c * 16;
+            tmem_load16(ta, t);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) t[i] *= alpha;
+            tmem_store16(ta, t);
+          }
+        }
+      }
+      // P row r, keys of this part: 64-key blocks of 16 KB, 128 bytes per
+      // row, 16-byte chunks swizzled by the row
+      const int kfirst = part * kPartKeys;
+      const uint32_t prow = sbase + C::kP0 + static_cast<uint32_t>(kfirst >> 6) * 16384u +
+                            static_cast<uint32_t>(r) * 128u;
+      const uint32_t sw = static_cast<uint32_t>(r & 7);
+#pragma unroll
+      for (int c = 0; c < kPartKeys / 8; ++c)
+        st_shared_u4(prow + ((static_cast<uint32_t>(((kfirst & 63) >> 3) + c) ^ sw) << 4),
+                     pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_full);
+    }
+    // the row sum of all parts (in part order), then O row / l
+    named_bar_sync(1 + (warp & 3), 32 * kRowSplit);
+    xch[part * 128 + r] = l;
+    named_bar_sync(1 + (warp & 3), 32 * kRowSplit);
+    l = 0.f;
+#pragma unroll
+    for (int q = 0; q < kRowSplit; ++q) l += xch[q * 128 + r];
+    wait(bar_pv, (nkt - 1) & 1);
+    if (ok) {
+      const float inv = 1.f / l;
+      const int b = b0 + r;
+      uint16_t* dst = a.o + (static_cast<size_t>(b) * a.H + h) * HD + part * kPartCols;
+#pragma unroll
+      for (int c = 0; c < kPartCols / 16; ++c) {
+        float t[16];
+        tmem_load16(tmem + lane_off + 256u + part * kPartCols + c * 16, t);
+        if (b < a.B) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            reinterpret_cast<uint4*>(dst + c * 16)[i] =
+                make_uint4(pack_bf16x2(t[8 * i] * inv, t[8 * i + 1] * inv),
+                           pack_bf16x2(t[8 * i + 2] * inv, t[8 * i + 3] * inv),
+                           pack_bf16x2(t[8 * i + 4] * inv, t[8 * i + 5] * inv),
+                           pack_bf16x2(t[8 * i + 6] * inv, t[8 * i + 7] * inv));
+        }
+      }
+    }
+  }
+
+  // On a timeout the producer may have copies in flight: let them land.
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int HD>
+pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          uint16_t* o, int B, int s, int H, int Hkv, cudaStream_t st,
+                          std::string* err) {
+  using C = AttnCfg<HD>;
+  static cudaError_t attr = cudaFuncSetAttribute(
+      attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+  if (attr != cudaSuccess) {
+    *err = std::string("attention shared-memory attribute: ") + cudaGetErrorString(attr);
+    return PDS_ELAUNCH;
+  }
+  const int T = s + B;
+  AttnMaps maps{};
+  pds_status rc;
+  if ((rc = tc_map_bf16(c, &maps.q, q, static_cast<uint64_t>(H) * HD, B, 128, err)) != PDS_OK)
+    return rc;
+  if ((rc = tc_map_bf16(c, &maps.k, k, static_cast<uint64_t>(Hkv) * HD, T, 128, err)) != PDS_OK)
+    return rc;
+  if ((rc = tc_map_bf16(c, &maps.v, v, static_cast<uint64_t>(Hkv) * HD, T, 128, err)) != PDS_OK)
+    return rc;
+  AttnArgs args{o, B, s, H, Hkv, 1.4426950408889634f / sqrtf(static_cast<float>(HD)), c.status};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(H, (B + kRows - 1) / kRows);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  if (c.pdl) {
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t ce = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, maps, args);
+  if (ce != cudaSuccess) {
+    *err = std::string("attention launch: ") + cudaGetErrorString(ce);
+    return PDS_ELAUNCH;
+  }
+  return PDS_OK;
+}
+
+}  // namespace
+
+pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
+                        std::string* err) {
+  // PDS_ATTN=mma selects the warp-level mma.sync kernel (a cross-check).
+  static const bool use_mma = [] {
+    const char* e = std::getenv("PDS_ATTN");
+    return e && std::string(e) == "mma";
+  }();
+  if (use_mma) return tc_attention_mma(c, q, k, v, o, B, start_pos, H, Hkv, hd, st, err);
+  return hd == 128 ? launch_attn_tc<128>(c, q, k, v, o, B, start_pos, H, Hkv, st, err)
+                   : launch_attn_tc<64>(c, q, k, v, o, B, start_pos, H, Hkv, st, err);
+}
+
+}  // namespace pds

@@ -1544,6 +1544,11 @@ pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t 
 
 }  // namespace
 
+pds_status tc_map_bf16(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner,
+                       uint64_t outer, uint32_t box_rows, std::string* err) {
+  return get_map(c, out, p, inner, outer, err, box_rows, 2);
+}
+
 size_t tc_gemm_scratch_bytes(int M, int max_tiles_n) {
   const size_t part_bytes = static_cast<size_t>(kGemmMaxGrid) * 2 * BM * 256 * sizeof(float);
   const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * max_tiles_n;

@@ -1,6 +1,7 @@
 // Tensor-core (tcgen05 / TMA) kernels of the stack: launch interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -47,6 +48,15 @@ pds_status tc_gemm_swiglu(TcContext& c, const uint16_t* A, const WeightRows& W, 
 size_t tc_gemm_noalloc_max_tiles();
 pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* C, int M, int N,
                                  int K, int num_sms, cudaStream_t st, std::string* err);
+// Tensor map of a row-major bf16 matrix [outer, inner]: boxes of 64 columns
+// (128 bytes, 128-byte swizzle) x box_rows rows; cached in c.maps.
+pds_status tc_map_bf16(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner,
+                       uint64_t outer, uint32_t box_rows, std::string* err);
+// GQA causal attention: the tcgen05 kernel (head_dim 64 or 128), or the
+// warp-level mma.sync kernel when PDS_ATTN=mma.
+pds_status tc_attention_mma(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            uint16_t* o, int B, int start_pos, int H, int Hkv, int hd,
+                            cudaStream_t st, std::string* err);
 pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
                         std::string* err);
