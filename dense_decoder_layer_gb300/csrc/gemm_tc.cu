@@ -296,11 +296,32 @@ __device__ __forceinline__ bool chunk_exists(const GemmArgs& g, int nt, int j) {
   return true;
 }
 
+// The (cos, sin) of this thread's row for RoPE channels 0..31, loaded while
+// the accumulator is still being made (channels 32..63 of a 128-wide head
+// are loaded into the same registers as the first ones are consumed).  The
+// table is laid out [channel][row]: one channel's rows are contiguous.
+struct RopeRegs {
+  float2 v[32];
+};
+__device__ __forceinline__ const float2* rope_row(const GemmArgs& g, int m) {
+  return g.qkv.rope + (m < g.M ? m : 0);
+}
+template <int BN>
+__device__ __forceinline__ void rope_prefetch(const GemmArgs& g, int nt, int ch, int m,
+                                              RopeRegs& rr) {
+  const QkvEpilogue& e = g.qkv;
+  if (nt * BN + ch * 128 >= e.q_width + e.kv_width) return;  // v columns: no rotation
+  const float2* cs = rope_row(g, m);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) rr.v[i] = __ldg(cs + static_cast<size_t>(i) * e.rope_ld);
+}
+
 // The fused epilogue of one tile for this thread (row `row` of the tile,
 // column half `ch`); r is the row's RMSNorm scale (SwiGLU and QKV).
 template <int BN, int EPI>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, int mt, int nt,
-                                             int row, int ch, int lane, float r, const Stage& st) {
+                                             int row, int ch, int lane, float r, const Stage& st,
+                                             RopeRegs& rr) {
   const int m = mt * BM + row;
   const bool live = m < g.M;
   const int m0w = mt * BM + (row & ~31);            // first row of this warp's 32
@@ -425,33 +446,49 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
                           : e.k_cache + static_cast<size_t>(e.start_pos + m0w) * e.kv_width +
                                 (c0 - e.q_width);
       const size_t ld = c0 < e.q_width ? e.q_width : e.kv_width;
-      // (cos, sin) table laid out [channel][row]: one channel's rows are contiguous
-      const float2* cs = e.rope + (live ? m : 0);
-#pragma unroll 1
-      for (int p = 0; p < 2; ++p) {
-        // head_dim 128: one head per 128 columns; channel i (< 64) pairs with
-        // i + 64, i.e. chunk p with chunk p + 2.  head_dim 64: two heads, chunk
-        // 2p with chunk 2p + 1.  The rotated halves are staged side by side
-        // (chunks 0-3 and 4-7 of the staging row) and stored together.
-        const int ja = (e.head_dim == 128) ? p : 2 * p;
-        const int jb = ja + half / 32;
-        const int i0 = (e.head_dim == 128) ? p * 32 : 0;
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          float va[16], vb[16];
-          acc_pair(taddr, ch * 4 + ja, h, ch * 4 + jb, h, va, vb);
+      // Channels cbase .. cbase + 15 of chunk pair (ja, jb), half h: rotate
+      // with the prefetched (cos, sin) and stage both rotated halves.
+      auto rotate = [&](int ja, int jb, int h, int cbase) {
+        float va[16], vb[16];
+        acc_pair(taddr, ch * 4 + ja, h, ch * 4 + jb, h, va, vb);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 sc = __ldg(cs + static_cast<size_t>(i0 + 16 * h + k) * e.rope_ld);
-            const float u = r * va[k], w = r * vb[k];
-            va[k] = u * sc.x - w * sc.y;
-            vb[k] = u * sc.y + w * sc.x;
-          }
-          stage_bf16(st, lane, 2 * h, va);
-          stage_bf16(st, lane, 4 + 2 * h, vb);
+        for (int k = 0; k < 16; ++k) {
+          const float2 sc = rr.v[cbase + k];
+          const float u = r * va[k], w = r * vb[k];
+          va[k] = u * sc.x - w * sc.y;
+          vb[k] = u * sc.y + w * sc.x;
         }
-        flush_bf16(st, 0, dst + ja * 32, ld, rows, lane);
-        flush_bf16(st, 4, dst + jb * 32, ld, rows, lane);
+        stage_bf16(st, lane, 2 * h, va);
+        stage_bf16(st, lane, 4 + 2 * h, vb);
+      };
+      // head_dim 128: one head per 128 columns; channel i (< 64) pairs with
+      // i + 64, i.e. chunk p with chunk p + 2.  head_dim 64: two heads, chunk
+      // 2p with chunk 2p + 1.  The rotated halves are staged side by side
+      // (chunks 0-3 and 4-7 of the staging row) and stored together.
+      if (e.head_dim == 128) {
+        // channels 0..31, reloading each 16 with channels 32.. once used
+        const float2* cs = rope_row(g, m);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          rotate(0, 2, h, 16 * h);
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            rr.v[16 * h + k] = __ldg(cs + static_cast<size_t>(32 + 16 * h + k) * e.rope_ld);
+        }
+        flush_bf16(st, 0, dst, ld, rows, lane);
+        flush_bf16(st, 4, dst + 2 * 32, ld, rows, lane);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) rotate(1, 3, h, 16 * h);
+        flush_bf16(st, 0, dst + 32, ld, rows, lane);
+        flush_bf16(st, 4, dst + 3 * 32, ld, rows, lane);
+      } else {
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) rotate(2 * p, 2 * p + 1, h, 16 * h);
+          flush_bf16(st, 0, dst + 2 * p * 32, ld, rows, lane);
+          flush_bf16(st, 4, dst + (2 * p + 1) * 32, ld, rows, lane);
+        }
       }
     }
   }
@@ -1106,10 +1143,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       unit_tile(g, unit, rank, mt, nt);
       // the row's RMSNorm scale, read while the accumulator is still being made
       float rscale = 0.f;
+      RopeRegs rr;
       if constexpr (EPI == kEpiSwiglu) {
         if (mt * BM + row < g.M) rscale = row_scale(g.swiglu.rs, mt * BM + row);
       } else if constexpr (EPI == kEpiQkv) {
         if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
+        rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
       }
       if (!mbar_wait(bar_tfull(ab), (sg >> 1) & 1, abort_flag, g.status)) break;
       tc_fence_after();
@@ -1185,7 +1224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ch * (BN / 64), BN / 64, 0, acc))
             break;
         } else {
-          run_epilogue<BN, EPI>(g, taddr, mt, nt, row, ch, lane, rscale, st);
+          run_epilogue<BN, EPI>(g, taddr, mt, nt, row, ch, lane, rscale, st, rr);
         }
         if (split && leader) g.counters[tile] = 0;
       }
