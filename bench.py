@@ -63,7 +63,8 @@ def flops(dims):
     return per, dims.n_layers * sum(per.values())
 
 
-KERNEL_SOURCES = ("gemm_tc.cu", "sm100.cuh", "attn.cu", "tc.h", "kernels.h", "common.cuh")
+KERNEL_SOURCES = ("gemm_tc.cu", "sm100.cuh", "attn_tc.cu", "attn.cu", "tc.h", "kernels.h",
+                  "common.cuh")
 
 
 def kernel_source_sha():
@@ -349,6 +350,10 @@ def main():
         "traffic": measured_traffic(dom, args.workload), "traffic_unit": "bytes per launch",
         "peak_source": f"{peak_src} bf16_tflops_sustained",
         "gemm_frac": gemm_flop / (gemm_ms / 1e3) / 1e12 / peak_tf,
+        # the GEMMs' share of the replayed step: the step less the other
+        # kernels' stand-alone times (launch gaps and overlaps go to the GEMMs)
+        "gemm_frac_in_step": gemm_flop / ((ms_per_step - sum(
+            kt[k][1] for k in kt if k not in gemm_kinds) / args.steps) / 1e3) / 1e12 / peak_tf,
         "end_to_end_frac": total_flop / (ms_per_step / 1e3) / 1e12 / peak_tf,
     }
 
