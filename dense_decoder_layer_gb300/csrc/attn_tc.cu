@@ -351,8 +351,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t sw = static_cast<uint32_t>(r & 7);
 #pragma unroll
       for (int c = 0; c < kPartKeys / 8; ++c)
-        st_shared_u4(prow + ((static_cast<uint32_t>(((kfirst & 63) >> 3) + c) ^ sw) << 4),
-                     pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        *reinterpret_cast<uint4*>(
+            smem + (prow - sbase) +
+            ((static_cast<uint32_t>(((kfirst & 63) >> 3) + c) ^ sw) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();

@@ -303,6 +303,13 @@ __device__ __forceinline__ bool chunk_exists(const GemmArgs& g, int nt, int j) {
 struct RopeRegs {
   float2 v[32];
 };
+// A (cos, sin) pair through the read-only path, as an opaque load: the
+// compiler must keep the value rather than issue the load again at its use.
+__device__ __forceinline__ float2 ld_rope(const float2* p) {
+  float2 v;
+  asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ const float2* rope_row(const GemmArgs& g, int m) {
   return g.qkv.rope + (m < g.M ? m : 0);
 }
@@ -313,7 +320,7 @@ __device__ __forceinline__ void rope_prefetch(const GemmArgs& g, int nt, int ch,
   if (nt * BN + ch * 128 >= e.q_width + e.kv_width) return;  // v columns: no rotation
   const float2* cs = rope_row(g, m);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) rr.v[i] = __ldg(cs + static_cast<size_t>(i) * e.rope_ld);
+  for (int i = 0; i < 32; ++i) rr.v[i] = ld_rope(cs + static_cast<size_t>(i) * e.rope_ld);
 }
 
 // The fused epilogue of one tile for this thread (row `row` of the tile,
@@ -473,7 +480,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
           rotate(0, 2, h, 16 * h);
 #pragma unroll
           for (int k = 0; k < 16; ++k)
-            rr.v[16 * h + k] = __ldg(cs + static_cast<size_t>(32 + 16 * h + k) * e.rope_ld);
+            rr.v[16 * h + k] = ld_rope(cs + static_cast<size_t>(32 + 16 * h + k) * e.rope_ld);
         }
         flush_bf16(st, 0, dst, ld, rows, lane);
         flush_bf16(st, 4, dst + 2 * 32, ld, rows, lane);
@@ -492,6 +499,14 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
       }
     }
   }
+}
+
+// A pointer into this CTA's shared memory for a shared-window address, so
+// that element accesses are ordinary (reorderable, batchable) C++ loads and
+// stores; sm is the dynamic shared memory at window address sbase.
+template <typename T>
+__device__ __forceinline__ T* sm_at(uint8_t* sm, uint32_t sbase, uint32_t addr) {
+  return reinterpret_cast<T*>(sm + (addr - sbase));
 }
 
 // Shared-memory address of epilogue box b of a CTA's last tile: the boxes
@@ -567,7 +582,8 @@ __device__ __forceinline__ void fixup_reduce_regs(const GemmArgs& g, const Fixup
 template <int BN, int EPI, bool PAIR>
 __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup& fx,
                                                   uint32_t taddr, int nt, int row, int ch,
-                                                  uint32_t sbase, int n_it, int box0) {
+                                                  uint8_t* sm, uint32_t sbase, int n_it,
+                                                  int box0) {
   using namespace sm100;
   constexpr int kOwned = owned_chunks<BN, EPI>();
   const int nother = fx.gl - fx.gf;  // contributors other than this CTA's group
@@ -621,7 +637,7 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
                           static_cast<uint32_t>(row) * 16u;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float4 p = ld_shared_f4(pb + q * BM * 16u);
+        const float4 p = *sm_at<float4>(sm, sbase, pb + q * BM * 16u);
         v[4 * q] += p.x;
         v[4 * q + 1] += p.y;
         v[4 * q + 2] += p.z;
@@ -646,7 +662,8 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
 template <int BN, bool PAIR, typename Acc>
 __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const GemmMaps& maps,
                                                     int mt, int nt, int row, int ch, int lane,
-                                                    uint32_t sbase, int n_it, uint32_t bar_res0,
+                                                    uint8_t* sm, uint32_t sbase, int n_it,
+                                                    uint32_t bar_res0,
                                                     volatile int* abort_flag, const Stage& st,
                                                     float* gain_sm, int jbeg, int jcnt,
                                                     int box_base, Acc&& acc) {
@@ -684,27 +701,30 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
       __syncwarp();
     }
     float t[8];
+    float4 rr[8];  // the residual row's 32 columns, all loads in flight at once
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      rr[q] = *sm_at<float4>(sm, sbase, rrow + ((static_cast<uint32_t>(q) ^ sw) << 4));
 #pragma unroll
     for (int q2 = 0; q2 < 4; ++q2) {
       float4 h[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int q = 2 * q2 + u;
-        const uint32_t addr = rrow + ((static_cast<uint32_t>(q) ^ sw) << 4);
-        const float4 r = ld_shared_f4(addr);
+        const float4 r = rr[q];
         h[u] = make_float4(r.x + v[4 * q], r.y + v[4 * q + 1], r.z + v[4 * q + 2],
                            r.w + v[4 * q + 3]);
-        st_shared_f4(addr, h[u]);
+        *sm_at<float4>(sm, sbase, rrow + ((static_cast<uint32_t>(q) ^ sw) << 4)) = h[u];
         t[q] = sumsq4(h[u]);
       }
       if (e.gain) {
         const float4 ga = gs[c * 8 + 2 * q2], gb = gs[c * 8 + 2 * q2 + 1];
         const uint32_t ac = static_cast<uint32_t>((j & 1) * 4 + q2);
-        st_shared_u4(a_stage + static_cast<uint32_t>(lane) * 128u + ((ac ^ sw) << 4),
-                     pack_bf16x2(h[0].x * ga.x, h[0].y * ga.y),
-                     pack_bf16x2(h[0].z * ga.z, h[0].w * ga.w),
-                     pack_bf16x2(h[1].x * gb.x, h[1].y * gb.y),
-                     pack_bf16x2(h[1].z * gb.z, h[1].w * gb.w));
+        *sm_at<uint4>(sm, sbase, a_stage + static_cast<uint32_t>(lane) * 128u + ((ac ^ sw) << 4)) =
+            make_uint4(pack_bf16x2(h[0].x * ga.x, h[0].y * ga.y),
+                       pack_bf16x2(h[0].z * ga.z, h[0].w * ga.w),
+                       pack_bf16x2(h[1].x * gb.x, h[1].y * gb.y),
+                       pack_bf16x2(h[1].z * gb.z, h[1].w * gb.w));
       }
     }
     // the 32 columns' sum in the register path's shuffle-tree order
@@ -763,7 +783,8 @@ __device__ __forceinline__ int split_recv_box(int S, int q, const SplitSlice& sl
 template <int BN>
 __device__ __forceinline__ bool split_resid_epilogue(
     const GemmArgs& g, const GemmMaps& maps, uint32_t taddr, int mt, int nt, int row, int ch,
-    int lane, uint32_t sbase, int grp, uint32_t bar_res0, uint32_t bar_ready, uint32_t bar_recv,
+    int lane, uint8_t* sm, uint32_t sbase, int grp, uint32_t bar_res0, uint32_t bar_ready,
+    uint32_t bar_recv,
     volatile int* abort_flag, const Stage& st, float* gain_sm, uint32_t crank, bool leader) {
   using namespace sm100;
   static_assert(BN == 256, "eight 32-column chunks in four 64-column units");
@@ -810,8 +831,8 @@ __device__ __forceinline__ bool split_resid_epilogue(
         const uint32_t src = src_box + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          st_shared_f4(src + ((static_cast<uint32_t>(q4) ^ sw) << 4),
-                       make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
+          *sm_at<float4>(sm, sbase, src + ((static_cast<uint32_t>(q4) ^ sw) << 4)) =
+              make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0)
@@ -843,7 +864,7 @@ __device__ __forceinline__ bool split_resid_epilogue(
                              static_cast<uint32_t>(row) * 128u;
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 x = ld_shared_f4(src + ((static_cast<uint32_t>(q4) ^ sw) << 4));
+          const float4 x = *sm_at<float4>(sm, sbase, src + ((static_cast<uint32_t>(q4) ^ sw) << 4));
           v[4 * q4] += x.x;
           v[4 * q4 + 1] += x.y;
           v[4 * q4 + 2] += x.z;
@@ -856,8 +877,9 @@ __device__ __forceinline__ bool split_resid_epilogue(
   const int half_cnt = mine.count >= 4 ? mine.count / 2 : (ch == 0 ? mine.count : 0);
   const int jbeg = mine.first + (mine.count >= 4 ? ch * (mine.count / 2) : 0);
   if (half_cnt == 0) return true;
-  return resid_epilogue_smem<BN, PAIR>(g, maps, mt, nt, row, ch, lane, sbase, my_n_it, bar_res0,
-                                       abort_flag, st, gain_sm, jbeg, half_cnt, mine.first, acc);
+  return resid_epilogue_smem<BN, PAIR>(g, maps, mt, nt, row, ch, lane, sm, sbase, my_n_it,
+                                       bar_res0, abort_flag, st, gain_sm, jbeg, half_cnt,
+                                       mine.first, acc);
 }
 
 template <int BN, int EPI, bool PAIR>
@@ -1161,7 +1183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g.split > 1) {
           // the CTA's only tile, finished with the cluster's other pairs
           const bool ok = split_resid_epilogue<BN>(
-              g, maps, taddr, mt, nt, row, ch, lane, sbase, grp, bar_res0, bar_ready, bar_recv,
+              g, maps, taddr, mt, nt, row, ch, lane, smem, sbase, grp, bar_res0, bar_ready, bar_recv,
               abort_flag, st, reinterpret_cast<float*>(smem + S * C::kStage + 1024), crank, leader);
           tc_fence_before();
           __syncwarp();
@@ -1209,7 +1231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // drained stages (after the residual boxes of a residual GEMM).
         if (split) {
           if (last) {
-            fixup_reduce_smem<BN, EPI, PAIR>(g, fx, taddr, nt, row, ch, sbase, it1 - it0,
+            fixup_reduce_smem<BN, EPI, PAIR>(g, fx, taddr, nt, row, ch, smem, sbase, it1 - it0,
                                              EPI == kEpiResid ? C::kResBoxes : 0);
           } else {
             fixup_reduce_regs<BN, EPI>(g, fx, taddr, nt, row, ch);
@@ -1218,7 +1240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (EPI == kEpiResid && last) {
           auto acc = [&](int j, float (&v)[32]) { tmem_load32(taddr + j * 32, v); };
-          if (!resid_epilogue_smem<BN, PAIR>(g, maps, mt, nt, row, ch, lane, sbase, it1 - it0,
+          if (!resid_epilogue_smem<BN, PAIR>(g, maps, mt, nt, row, ch, lane, smem, sbase, it1 - it0,
                                              bar_res0, abort_flag, st,
                                              reinterpret_cast<float*>(smem + S * C::kStage + 1024),
                                              ch * (BN / 64), BN / 64, 0, acc))
