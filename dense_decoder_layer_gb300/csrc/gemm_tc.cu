@@ -330,7 +330,6 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
                                              int row, int ch, int lane, float r, const Stage& st,
                                              RopeRegs& rr) {
   const int m = mt * BM + row;
-  const bool live = m < g.M;
   const int m0w = mt * BM + (row & ~31);            // first row of this warp's 32
   const int rows = max(0, min(32, g.M - m0w));      // of which exist
   if constexpr (EPI == kEpiPlain || EPI == kEpiResid) {
@@ -428,7 +427,6 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
   } else {
     static_assert(BN == 256, "the QKV tile holds whole heads in each 128-column half");
     const QkvEpilogue& e = g.qkv;
-    const int half = e.head_dim / 2;
     const int c0 = nt * BN + ch * 128;  // this thread's 128 columns of [q | k | v]
     if (c0 >= e.q_width + 2 * e.kv_width) return;
     if (c0 >= e.q_width + e.kv_width) {
@@ -650,7 +648,8 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
 }
 
 // Residual epilogue of a CTA's last tile, through shared memory, for this
-// thread's 32-column chunks jbeg .. jbeg + jcnt - 1 (jbeg even).  The
+// thread's 32-column chunks jbeg .. jbeg + jcnt - 1 (jbeg even); gain_sm
+// holds the tile's BN gains (see resid_gain_prefetch).  The
 // producer has loaded the residual boxes of chunks box_base .. into the
 // drained stages (box j - box_base, one barrier per stage).  Each thread
 // takes its row's accumulator from acc(j, v) (TMEM, or TMEM plus the other
@@ -677,14 +676,8 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
   const uint64_t pol_keep = policy_evict_last();
   const uint32_t sw = static_cast<uint32_t>(row & 7);
   const uint32_t a_stage = smem_u32(st.base);  // this warp's 32 rows x 64 bf16 of the operand
-  // The gain of this thread's columns, once, by the half's first warp.
-  if (e.gain) {
-    if (lane_grp == 0 && lane < jcnt * 8)
-      reinterpret_cast<float4*>(gain_sm)[ch * (BN / 8) + lane] =
-          __ldg(reinterpret_cast<const float4*>(e.gain + nt * BN + jbeg * 32) + lane);
-    named_bar_sync(2 + ch, 128);
-  }
-  const float4* gs = reinterpret_cast<const float4*>(gain_sm) + ch * (BN / 8);
+  // the tile's gain, loaded into shared memory before the accumulator wait
+  const float4* gs = reinterpret_cast<const float4*>(gain_sm);
   float ss = 0.f;
 #pragma unroll 1
   for (int c = 0; c < jcnt; ++c) {
@@ -718,7 +711,7 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
         t[q] = sumsq4(h[u]);
       }
       if (e.gain) {
-        const float4 ga = gs[c * 8 + 2 * q2], gb = gs[c * 8 + 2 * q2 + 1];
+        const float4 ga = gs[j * 8 + 2 * q2], gb = gs[j * 8 + 2 * q2 + 1];
         const uint32_t ac = static_cast<uint32_t>((j & 1) * 4 + q2);
         *sm_at<uint4>(sm, sbase, a_stage + static_cast<uint32_t>(lane) * 128u + ((ac ^ sw) << 4)) =
             make_uint4(pack_bf16x2(h[0].x * ga.x, h[0].y * ga.y),
@@ -749,6 +742,18 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
   }
   __syncwarp();
   return true;
+}
+
+// The gains of the BN columns of column tile nt into shared memory, by the
+// epilogue threads, before they wait for the CTA's last accumulator (the
+// gain is a weight: it does not wait for the previous kernel).
+template <int BN>
+__device__ __forceinline__ void resid_gain_prefetch(const GemmArgs& g, int nt, float* gain_sm,
+                                                    int et) {
+  if (g.resid.gain && et < BN / 4)
+    reinterpret_cast<float4*>(gain_sm)[et] =
+        __ldg(reinterpret_cast<const float4*>(g.resid.gain + nt * BN) + et);
+  sm100::named_bar_sync(1, kEpiThreads);
 }
 
 // Cluster split-K of a residual GEMM: the cluster's S pairs compute one
@@ -1171,6 +1176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (EPI == kEpiQkv) {
         if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
         rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
+      } else if constexpr (EPI == kEpiResid) {
+        // the last tile's epilogue goes through shared memory and reads its gains there
+        if (si.it >= si.end)
+          resid_gain_prefetch<BN>(g, nt, reinterpret_cast<float*>(smem + S * C::kStage + 1024),
+                                  static_cast<int>(threadIdx.x) - kEpiFirstThread);
       }
       if (!mbar_wait(bar_tfull(ab), (sg >> 1) & 1, abort_flag, g.status)) break;
       tc_fence_after();
