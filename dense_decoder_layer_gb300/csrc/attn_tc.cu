@@ -360,7 +360,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_full);
     }
-    // the row sum of all parts (in part order), then O row / l
+    // the row sum of all parts (in part order), while the last P.V runs;
+    // then O row / l
     named_bar_sync(1 + (warp & 3), 32 * kRowSplit);
     xch[part * 128 + r] = l;
     named_bar_sync(1 + (warp & 3), 32 * kRowSplit);
