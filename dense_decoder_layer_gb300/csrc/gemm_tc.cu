@@ -1,16 +1,25 @@
-// Persistent stream-K tcgen05 GEMM with the stack's fused epilogues.
+// Persistent tcgen05 GEMM with the stack's fused epilogues.
 //
 //   C[M, N] = A[M, K] . W[N, K]^T      A, W bf16 (K contiguous), fp32 accumulate
 //
-// One CTA per SM (320 threads, ~226 KB of shared memory, 2*BN TMEM columns):
-//   warp 0      TMA producer: A box [128 x 64] and W boxes [128 x 64] per
-//               k-block into a ring of S shared-memory stages (128-byte swizzle)
-//   warp 1      tcgen05.mma issuer (one thread): 128 x BN x 16 steps into a
-//               double-buffered TMEM accumulator; commits free the stages
-//   warps 2..9  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+// One CTA per SM (384 threads, ~227 KB of shared memory, 2*BN TMEM columns):
+//   warp 0      TMA producer: the A box [128 x 64] and the W boxes of each
+//               k-block into a ring of S shared-memory stages (128-byte
+//               swizzle); weight boxes of the first stages go out before the
+//               previous kernel has finished (programmatic dependent launch)
+//   warp 1      tcgen05.mma issuer (one thread) into a double-buffered TMEM
+//               accumulator; commits free the stages
+//   warps 4..11 epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
 //               output row; two warps per lane group split the columns),
-//               a warp-private shared-memory transpose, then the fused
-//               epilogue with row-contiguous global loads and stores
+//               then the fused epilogue (a warp-private shared-memory
+//               transpose and row-contiguous stores, or, for a residual
+//               GEMM's last tile, shared memory and TMA throughout)
+// Warpgroup 0 lowers its registers with setmaxnreg so the epilogue
+// warpgroups can hold their fused epilogues without spilling.
+//
+// CTA pairs: when the row tiles come in pairs, the two CTAs of a cluster
+// compute a 256 x BN tile with cta_group::2 MMAs; each loads its own 128
+// rows of A and half of the BN weight rows, and the even CTA issues the MMAs.
 //
 // Work split (grouped stream-K): CTAs form groups of gs (a divisor of the
 // row-tile count, up to 8) that take the same (column tile, k-block) ranges
@@ -19,9 +28,15 @@
 // into equal contiguous ranges, one per group.  A tile whose k-blocks are
 // spread over several groups is finished by the last CTA to arrive: each
 // stores its float32 partial tile to scratch and bumps the tile's counter;
-// the one that sees the final count adds all partials in k order (the sum is
-// the same whoever arrives last) and runs the epilogue.  No CTA ever waits
-// for another.
+// the one that sees the final count adds the others' partials and its own
+// accumulator in k order into its TMEM accumulator (the sum is the same
+// whoever arrives last) and runs the epilogue.  No CTA ever waits for
+// another.
+//
+// Cluster split-K (residual GEMMs with few pair tiles): a cluster of 2S CTAs
+// computes one 256 x BN tile, pair q over the q-th of S k ranges; the pairs
+// exchange column slices of their accumulators through distributed shared
+// memory and each finishes its own slice (see split_resid_epilogue).
 //
 // Epilogues (the stack's fusions; frink-models 0.29.0
 // src/decoder/cuda_prefill.rs, module doc: everything between the seven
