@@ -21,12 +21,23 @@
 //               TMEM is then rescaled once), so exp2 values stay <= 256.  At
 //               the end the quarters add their row sums in order and each
 //               divides and stores a quarter of the O row.
-// S_{j+1} is computed while the softmax works on S_j.  Every wait is
-// bounded; a wait that gives up sets the status word and the CTA exits.
+// S_{j+1} is computed while the softmax works on S_j.
+//
+// Key-range split: when there are fewer query tiles than SMs, the heaviest
+// tiles with long key ranges (as many as fit one CTA per SM) are computed by
+// the two CTAs of a cluster, each over half of the tile's key range.  The second CTA sends its
+// unnormalised O, row maxima and row sums into the first one's drained
+// shared memory (bulk copies), and the first combines the halves in a fixed
+// order: O = O0 2^(m0-m) + O1 2^(m1-m) over l0 2^(m0-m) + l1 2^(m1-m).
+//
+// Every wait is bounded; a wait that gives up sets the status word and the
+// CTA exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdlib>
+#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -44,6 +55,11 @@ constexpr int kSoftmaxFirstWarp = 4;
 constexpr int kSoftmaxThreads = 128 * kRowSplit;
 constexpr int kAttnThreads = 32 * kSoftmaxFirstWarp + kSoftmaxThreads;
 constexpr float kRescaleLog2 = 8.0f;  // move the reference max beyond a 2^8 growth
+// Shortest key range (in 128-key tiles) worth splitting over a CTA pair: the
+// second CTA's prologue and the merge cost about three key tiles (measured:
+// splitting 4-tile ranges made the kernel slower, 12.8 -> 14.1 us at 24 heads
+// x 512 rows; splitting 15- and 16-tile ranges faster, 26.8 -> 25.2 us).
+constexpr int kSplitMinKeyTiles = 8;
 
 template <int HD>
 struct AttnCfg {
@@ -55,7 +71,7 @@ struct AttnCfg {
   static constexpr uint32_t kP0 = kV0 + 2u * kTile;  // one P buffer
   static constexpr uint32_t kX = kP0 + kP;           // row maxima / sums of the halves
   static constexpr uint32_t kBar = kX + 2u * kRowSplit * 128u * 4u;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 18;
   static constexpr size_t kSmem = 1024 + kBar + kNumBars * 8 + 16;
   static_assert(kSmem <= 232448, "shared memory per CTA");
   // TMEM: S buffers at columns 0 and 128, O at 256
@@ -70,6 +86,7 @@ struct AttnArgs {
   int B, s, H, Hkv;
   float scale_log2;
   uint32_t* status;
+  int n_split;  // the first (heaviest) n_split tiles are split over a CTA pair
 };
 
 // K-major SW128 descriptor of a 128-row operand whose K extent is split in
@@ -146,15 +163,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t bar_p_full = bar0 + 8u * 13;  // phase j: P_j is in shared memory
   const uint32_t bar_pv = bar0 + 8u * 14;      // phase j: O += P_j V_j has completed
   const uint32_t bar_drain = bar0 + 8u * 15;   // every MMA of the CTA has completed
+  const uint32_t bar_m_ready = bar0 + 8u * 16;  // split, second CTA: the first may receive
+  const uint32_t bar_m_recv = bar0 + 8u * 17;   // split, first CTA: the second's half landed
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kBar + C::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = gridDim.y - 1 - blockIdx.y;  // longest row tiles first
-  const int h = blockIdx.x, g = h / (a.H / a.Hkv);
+  // Tiles t = 0, 1, ... run from the longest query tiles to the shortest
+  // (head fastest).  With gridDim.x = 2 (clusters of 2 CTAs) cluster c < n_split
+  // computes tile c with its key range split in halves, and every later
+  // cluster two whole tiles, one per CTA.
+  const int nq = (a.B + kRows - 1) / kRows;
+  int t = blockIdx.y, half = 0;
+  bool split = false;
+  if (gridDim.x == 2) {
+    half = static_cast<int>(cluster_rank());
+    if (t < a.n_split) {
+      split = true;
+    } else {
+      t = a.n_split + 2 * (t - a.n_split) + half;
+      half = 0;
+      if (t >= a.H * nq) return;
+    }
+  }
+  const int qt = nq - 1 - t / a.H;
+  const int h = t % a.H, g = h / (a.H / a.Hkv);
   const int b0 = qt * kRows;
   const int last_row = min(b0 + kRows, a.B) - 1;
-  const int nkt = (a.s + last_row + 1 + kKeys - 1) / kKeys;  // key tiles this CTA reads
+  const int nkt = (a.s + last_row + 1 + kKeys - 1) / kKeys;  // key tiles of the query tile
+  const int nk0 = (nkt + 1) / 2;
+  const int kt0 = (split && half == 1) ? nk0 : 0;                   // first key tile of this CTA
+  const int n = split ? (half == 0 ? nk0 : nkt - nk0) : nkt;        // its key tiles
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -169,6 +208,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(bar_p_full, kSoftmaxThreads / 32);
     mbar_init(bar_pv, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_m_ready, 1);
+    mbar_init(bar_m_recv, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -184,6 +225,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (split) cluster_sync();  // the peer's barriers are initialised before any remote arrive
   const uint32_t tmem = misc[0];
   grid_dep_launch();
 
@@ -204,12 +246,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive_expect_tx(full + 8u * st, C::kTile);
         for (int c = 0; c < HD / 64; ++c)
           tma_load_2d(base + st * C::kTile + c * 16384u, map, full + 8u * st, g * HD + c * 64,
-                      j * kKeys, pol);
+                      (kt0 + j) * kKeys, pol);
         return true;
       };
       bool ok = load(&maps.k, sbase + C::kK0, bar_k_full(0), bar_k_empty(0), 0);
-      for (int j = 0; ok && j < nkt; ++j) {
-        if (j + 1 < nkt && !(ok = load(&maps.k, sbase + C::kK0, bar_k_full(0), bar_k_empty(0), j + 1)))
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n && !(ok = load(&maps.k, sbase + C::kK0, bar_k_full(0), bar_k_empty(0), j + 1)))
           break;
         ok = load(&maps.v, sbase + C::kV0, bar_v_full(0), bar_v_empty(0), j);
       }
@@ -236,8 +278,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         return true;
       };
       if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < nkt; ++j) {
-        if (j + 1 < nkt && !(ok = issue_s(j + 1))) break;
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n && !(ok = issue_s(j + 1))) break;
         const int st = j & 1;
         if (!(ok = mbar_wait(bar_v_full(st), (j >> 1) & 1, abort_flag, a.status))) break;
         if (!(ok = mbar_wait(bar_p_full, j & 1, abort_flag, a.status))) break;
@@ -260,8 +302,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int r = (sw_idx & 3) * 32 + lane;                 // query row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* xch = reinterpret_cast<float*>(smem + C::kX);   // [2 tiles][parts][128 rows]
-    const int pos = a.s + b0 + r;
     constexpr int kPartKeys = kKeys / kRowSplit;
+    // the row's position less the first key of this part of key tile 0
+    const int rel0 = a.s + b0 + r - (kt0 * kKeys + part * kPartKeys);
     constexpr int kPartCols = HD / kRowSplit;
     static_assert(kPartKeys % 32 == 0 && kPartCols % 16 == 0, "TMEM loads of the parts");
     const float sc = a.scale_log2;
@@ -276,7 +319,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) tc_fence_after();
     };
-    for (int j = 0; j < nkt; ++j) {
+    for (int j = 0; j < n; ++j) {
       const int st = j & 1;
       wait(bar_s_full(st), (j >> 1) & 1);
       float sv[kPartKeys];
@@ -293,11 +336,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_s_free(st));
         // causal mask and this part's maximum
-        const int key0 = j * kKeys + part * kPartKeys;
-        if (key0 + kPartKeys - 1 > a.s + b0) {  // some key past some row
+        const int rel = rel0 - j * kKeys;  // key i of the part is past the row: i > rel
+        if (kPartKeys - 1 > rel - r) {      // some key past some row of the tile
 #pragma unroll
           for (int i = 0; i < kPartKeys; ++i)
-            if (key0 + i > pos) sv[i] = -INFINITY;
+            if (i > rel) sv[i] = -INFINITY;
         }
         mx = tree_max<kPartKeys>(sv);
       }
@@ -311,18 +354,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float alpha = 1.f;
       bool rescale = false;
       if (j == 0) {
-        m_ref = mxs;  // key 0 is visible to every row: finite
-      } else if (mxs > m_ref + kRescaleLog2) {
+        m_ref = mxs;  // -inf while no key of the CTA's range is visible to the row
+      } else if (mxs > m_ref + kRescaleLog2) {  // also from -inf (alpha 0; O and l are 0)
         alpha = exp2f(m_ref - mxs);
         m_ref = mxs;
         rescale = true;
       }
       // P = exp2(s * scale - m_ref) as bf16, and this part's row sum
       uint32_t pk[kPartKeys / 2];
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // masked scores give 0
 #pragma unroll
       for (int i = 0; i < kPartKeys / 2; ++i) {
-        sv[2 * i] = exp2_sfu(fmaf(sv[2 * i], sc, -m_ref));
-        sv[2 * i + 1] = exp2_sfu(fmaf(sv[2 * i + 1], sc, -m_ref));
+        sv[2 * i] = exp2_sfu(fmaf(sv[2 * i], sc, -m_use));
+        sv[2 * i + 1] = exp2_sfu(fmaf(sv[2 * i + 1], sc, -m_use));
         pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
       }
       const float sum = tree_sum<kPartKeys>(sv);
@@ -368,8 +412,84 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     l = 0.f;
 #pragma unroll
     for (int q = 0; q < kRowSplit; ++q) l += xch[q * 128 + r];
-    wait(bar_pv, (nkt - 1) & 1);
-    if (ok) {
+    wait(bar_pv, (n - 1) & 1);
+    // split: the second CTA's O part (float32, 16-byte chunks swizzled by the
+    // row) goes to the first CTA at the K stages' offset, its row sum and
+    // row maximum at the P buffer's offset
+    constexpr int kPartChunks = kPartCols / 4;
+    const uint32_t o_row = C::kK0 + static_cast<uint32_t>((part * 128 + r) * kPartCols * 4);
+    auto o_chunk = [&](int c) {
+      return o_row + (static_cast<uint32_t>(c ^ (r & (kPartChunks - 1))) << 4);
+    };
+    float* lmsg = reinterpret_cast<float*>(smem + C::kP0);  // [128] row sums, then [128] maxima
+    if (split && half == 1) {
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < kPartCols / 16; ++c) {
+          float t[16];
+          tmem_load16(tmem + lane_off + 256u + part * kPartCols + c * 16, t);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4*>(smem + o_chunk(4 * c + i)) =
+                make_float4(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
+        }
+        if (part == 0) {
+          lmsg[r] = l;
+          lmsg[128 + r] = m_ref;
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      wait(bar_m_ready, 0);
+      if (ok && lane == 0) {
+        const uint32_t rbar = mapa_shared(bar_m_recv, 0);
+        const uint32_t rows0 = static_cast<uint32_t>((warp & 3) * 32);  // this warp's rows
+        const uint32_t o_off = sbase + C::kK0 + (part * 128u + rows0) * kPartCols * 4u;
+        bulk_copy_to_cluster(mapa_shared(o_off, 0), o_off, 32u * kPartCols * 4u, rbar);
+        if (part == 0) {
+          const uint32_t l_off = sbase + C::kP0 + rows0 * 4u;
+          bulk_copy_to_cluster(mapa_shared(l_off, 0), l_off, 128u, rbar);
+          bulk_copy_to_cluster(mapa_shared(l_off + 512u, 0), l_off + 512u, 128u, rbar);
+        }
+      }
+    } else if (split) {
+      if (ok && threadIdx.x == kSoftmaxFirstWarp * 32) {
+        mbar_arrive_expect_tx(bar_m_recv, 128u * HD * 4u + 1024u);
+        mbar_arrive_cluster(mapa_shared(bar_m_ready, 1));  // O, P and K are done with here
+      }
+      wait(bar_m_recv, 0);
+      if (ok) {
+        const float m1 = lmsg[128 + r];
+        const float m = fmaxf(m_ref, m1);  // m_ref: key 0 is in the first half, finite
+        const float a0 = exp2f(m_ref - m);
+        const float a1 = m1 == -INFINITY ? 0.f : exp2f(m1 - m);
+        const float inv = 1.f / (l * a0 + lmsg[r] * a1);
+        const int b = b0 + r;
+        uint16_t* dst = a.o + (static_cast<size_t>(b) * a.H + h) * HD + part * kPartCols;
+#pragma unroll
+        for (int c = 0; c < kPartCols / 16; ++c) {
+          float t[16];
+          tmem_load16(tmem + lane_off + 256u + part * kPartCols + c * 16, t);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 o1 = *reinterpret_cast<const float4*>(smem + o_chunk(4 * c + i));
+            t[4 * i] = (t[4 * i] * a0 + o1.x * a1) * inv;
+            t[4 * i + 1] = (t[4 * i + 1] * a0 + o1.y * a1) * inv;
+            t[4 * i + 2] = (t[4 * i + 2] * a0 + o1.z * a1) * inv;
+            t[4 * i + 3] = (t[4 * i + 3] * a0 + o1.w * a1) * inv;
+          }
+          if (b < a.B) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              reinterpret_cast<uint4*>(dst + c * 16)[i] =
+                  make_uint4(pack_bf16x2(t[8 * i], t[8 * i + 1]),
+                             pack_bf16x2(t[8 * i + 2], t[8 * i + 3]),
+                             pack_bf16x2(t[8 * i + 4], t[8 * i + 5]),
+                             pack_bf16x2(t[8 * i + 6], t[8 * i + 7]));
+          }
+        }
+      }
+    } else if (ok) {
       const float inv = 1.f / l;
       const int b = b0 + r;
       uint16_t* dst = a.o + (static_cast<size_t>(b) * a.H + h) * HD + part * kPartCols;
@@ -399,7 +519,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // a split pair: neither CTA leaves while the other may still copy into it
+  if (split) cluster_sync();
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// Clusters of two attention CTAs that fit on the GPU at once.
+template <int HD>
+int attn_max_pairs(const cudaLaunchConfig_t& base) {
+  static std::mutex mu;
+  static int pairs = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pairs) {
+    cudaLaunchAttribute ca[1];
+    ca[0].id = cudaLaunchAttributeClusterDimension;
+    ca[0].val.clusterDim.x = 2;
+    ca[0].val.clusterDim.y = 1;
+    ca[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t q = base;
+    q.gridDim = dim3(2);
+    q.attrs = ca;
+    q.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<HD>, &q) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 0;  // no pairs: no split
+    }
+    pairs = n;
+  }
+  return pairs;
 }
 
 template <int HD>
@@ -422,19 +570,44 @@ pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, co
     return rc;
   if ((rc = tc_map_bf16(c, &maps.v, v, static_cast<uint64_t>(Hkv) * HD, T, 128, err)) != PDS_OK)
     return rc;
-  AttnArgs args{o, B, s, H, Hkv, 1.4426950408889634f / sqrtf(static_cast<float>(HD)), c.status};
+  AttnArgs args{o, B, s, H, Hkv, 1.4426950408889634f / sqrtf(static_cast<float>(HD)), c.status,
+                0};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(H, (B + kRows - 1) / kRows);
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  if (c.pdl) {
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
+  // Split the longest query tiles (a whole row of tiles over the heads at a
+  // time) while every CTA still has an SM of its own: fewer tiles than SMs
+  // otherwise leave SMs idle behind the longest tiles.
+  const int nq = (B + kRows - 1) / kRows, tiles = H * nq;
+  const int pair_cap = std::min(c.num_sms / 2, attn_max_pairs<HD>(cfg));
+  int n_split = 0;
+  for (int qt = nq - 1; qt >= 0; --qt) {
+    const int nkt = (s + std::min((qt + 1) * kRows, B) + kKeys - 1) / kKeys;
+    const int n = n_split + H;
+    if (nkt < kSplitMinKeyTiles || n + (tiles - n + 1) / 2 > pair_cap) break;
+    n_split = n;
   }
+  args.n_split = n_split;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (n_split > 0) {
+    cfg.gridDim = dim3(2, n_split + (tiles - n_split + 1) / 2);
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = 2;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  } else {
+    cfg.gridDim = dim3(1, tiles);
+  }
+  if (c.pdl) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
   cudaError_t ce = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, maps, args);
   if (ce != cudaSuccess) {
     *err = std::string("attention launch: ") + cudaGetErrorString(ce);

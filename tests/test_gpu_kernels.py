@@ -40,7 +40,9 @@ def test_gemm_bf16_matches_fp64(M, N, K):
 @pytest.mark.parametrize("B,s,H,Hkv,hd", [(1, 0, 4, 2, 64), (7, 0, 4, 2, 64), (130, 0, 8, 2, 64),
                                           (64, 100, 6, 2, 128), (200, 333, 3, 1, 128),
                                           (1, 77, 8, 8, 128), (512, 1536, 24, 8, 128),
-                                          (129, 0, 32, 8, 64)])
+                                          (129, 0, 32, 8, 64),
+                                          # key ranges of 9-11 tiles, split over CTA pairs
+                                          (300, 1000, 4, 2, 64), (130, 900, 5, 1, 128)])
 def test_attention_matches_oracle(B, s, H, Hkv, hd):
     from dense_decoder_layer_gb300 import pds
     rng = np.random.default_rng(B + 11 * s + H)
