@@ -24,6 +24,7 @@ struct Plan {
   int device = -1;
   int num_sms = 0;
   uint32_t* d_status = nullptr;  // status word written by bounded device waits
+  uint32_t* h_status = nullptr;  // pinned host copy of it, read after a stream synchronize
   TmapCache* maps = nullptr;  // encoded TMA descriptors, reused across calls
   // Per-kernel timing (pds_plan_set_timing).
   bool timing = false;

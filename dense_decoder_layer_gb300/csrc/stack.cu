@@ -50,11 +50,15 @@ pds_status ensure_device_state(Plan& p, std::string* err) {
   ce = cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (ce == cudaSuccess) ce = cudaMalloc(&p.d_status, sizeof(uint32_t));
   if (ce == cudaSuccess) ce = cudaMemset(p.d_status, 0, sizeof(uint32_t));
+  if (ce == cudaSuccess) ce = cudaMallocHost(&p.h_status, sizeof(uint32_t));
   if (ce != cudaSuccess) {
     *err = std::string("plan device state: ") + cudaGetErrorString(ce);
+    if (p.d_status) cudaFree(p.d_status);
     p.d_status = nullptr;
+    p.h_status = nullptr;
     return PDS_ENOMEM;
   }
+  *p.h_status = 0;
   p.device = dev;
   if (!p.maps) p.maps = tmap_cache_create();
   return PDS_OK;
@@ -103,20 +107,29 @@ void plan_release_device(Plan& p) {
   p.events.clear();
   if (p.d_status) cudaFree(p.d_status);
   p.d_status = nullptr;
+  if (p.h_status) cudaFreeHost(p.h_status);
+  p.h_status = nullptr;
   if (p.maps) tmap_cache_destroy(p.maps);
   p.maps = nullptr;
 }
 
 pds_status plan_sync(Plan& p, cudaStream_t st, std::string* err) {
-  cudaError_t ce = cudaStreamSynchronize(st);
+  // the status word comes back on the stream, behind the call's work, so
+  // that one synchronize covers both
+  cudaError_t ce = cudaSuccess;
+  if (p.d_status && p.h_status)
+    ce = cudaMemcpyAsync(p.h_status, p.d_status, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
   if (ce != cudaSuccess) {
     *err = std::string("stream synchronize: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;
   }
-  if (!p.d_status) return PDS_OK;
-  uint32_t flags = 0;
-  ce = cudaMemcpy(&flags, p.d_status, sizeof(flags), cudaMemcpyDeviceToHost);
-  if (ce == cudaSuccess && flags) ce = cudaMemset(p.d_status, 0, sizeof(uint32_t));
+  if (!p.d_status || !p.h_status) return PDS_OK;
+  const uint32_t flags = *static_cast<volatile uint32_t*>(p.h_status);
+  if (flags) {
+    *p.h_status = 0;
+    ce = cudaMemset(p.d_status, 0, sizeof(uint32_t));
+  }
   if (ce != cudaSuccess) {
     *err = std::string("status word: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;

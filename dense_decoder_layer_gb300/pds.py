@@ -110,6 +110,8 @@ def check(status: int) -> None:
 
 
 def _ptrs(values):
+    if isinstance(values, ctypes.Array):  # already marshalled (see DenseStack)
+        return values
     arr = (ctypes.c_void_p * len(values))()
     for i, v in enumerate(values):
         arr[i] = v
@@ -133,6 +135,8 @@ def pds_workspace_bytes(plan, max_batch: int) -> int:
 
 
 def _layer_array(layers):
+    if isinstance(layers, ctypes.Array):  # already marshalled (see DenseStack)
+        return layers
     arr = (pds_layer * len(layers))()
     for i, l in enumerate(layers):
         for n in LAYER_FIELDS:
@@ -143,7 +147,8 @@ def _layer_array(layers):
 def pds_prefill_dense_stack(plan, layers, k_cache, v_cache, cache_capacity, start_pos, batch,
                             hidden_in, hidden_out, workspace, workspace_bytes, stream) -> None:
     """Host in/out call.  ``layers``: list of dicts field -> device pointer;
-    ``k_cache``/``v_cache``: lists of device pointers; ``hidden_in``/``hidden_out``:
+    ``k_cache``/``v_cache``: lists of device pointers (or the ctypes arrays that
+    ``_layer_array`` / ``_ptrs`` make); ``hidden_in``/``hidden_out``:
     host pointers."""
     check(load().pds_prefill_dense_stack(plan, _layer_array(layers), _ptrs(k_cache),
                                          _ptrs(v_cache), cache_capacity, start_pos, batch,

@@ -44,10 +44,14 @@ class DenseStack:
         self.k_cache = [torch.zeros(self.cache_capacity, kvw, dtype=torch.bfloat16,
                                     device=self.device) for _ in range(L)]
         self.v_cache = [torch.zeros_like(self.k_cache[0]) for _ in range(L)]
+        # the C arrays of pointers are built once, not on every call
+        self._k_ptrs = pds._ptrs([t.data_ptr() for t in self.k_cache])
+        self._v_ptrs = pds._ptrs([t.data_ptr() for t in self.v_cache])
         self.ws_bytes = pds.pds_workspace_bytes(self.plan, self.max_batch)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.weights = []
         self._layer_ptrs = []
+        self._layers_c = pds._layer_array([])
 
     def close(self):
         if self.plan is not None:
@@ -75,11 +79,13 @@ class DenseStack:
                     t[n] = torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(self.device)
             self.weights.append(t)
             self._layer_ptrs.append({n: t[n].data_ptr() for n in LAYER_FIELDS})
+        self._layers_c = pds._layer_array(self._layer_ptrs)
 
     def set_layer_tensors(self, layers) -> None:
         """Use device tensors the caller already holds (dicts field -> tensor)."""
         self.weights = list(layers)
         self._layer_ptrs = [{n: l[n].data_ptr() for n in LAYER_FIELDS} for l in layers]
+        self._layers_c = pds._layer_array(self._layer_ptrs)
 
     def load_prefix(self, prefix_k, prefix_v) -> None:
         """Rows [0, s) of every cache from bf16 bit arrays [s, Hkv, hd]."""
@@ -103,8 +109,8 @@ class DenseStack:
         if out is None:
             out = torch.empty_like(hidden)
         pds.pds_prefill_dense_stack(
-            self.plan, self._layer_ptrs, [t.data_ptr() for t in self.k_cache],
-            [t.data_ptr() for t in self.v_cache], self.cache_capacity, start_pos, B,
+            self.plan, self._layers_c, self._k_ptrs, self._v_ptrs, self.cache_capacity,
+            start_pos, B,
             hidden.data_ptr(), out.data_ptr(), self.workspace.data_ptr(), self.ws_bytes,
             self._stream(stream))
         return out
@@ -114,8 +120,8 @@ class DenseStack:
         """Device float32 [B, d] in and out, enqueued on the stream."""
         B = hidden.shape[0]
         pds.pds_prefill_dense_stack_device(
-            self.plan, self._layer_ptrs, [t.data_ptr() for t in self.k_cache],
-            [t.data_ptr() for t in self.v_cache], self.cache_capacity, start_pos, B,
+            self.plan, self._layers_c, self._k_ptrs, self._v_ptrs, self.cache_capacity,
+            start_pos, B,
             hidden.data_ptr(), out.data_ptr(), self.workspace.data_ptr(), self.ws_bytes,
             self._stream(stream))
 

@@ -124,3 +124,29 @@ def test_component_entry_points_validate_on_host():
     assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 4, 0, 4, 2, 96, None) == pds.PDS_DECLINED
     assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 4, 0, 5, 2, 64, None) == pds.PDS_DECLINED
     assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 0, 0, 4, 2, 64, None) == pds.PDS_EINVAL
+
+
+def test_stack_marshals_pointer_arrays_once():
+    """DenseStack hands the C ABI pointer arrays built once (not per call);
+    they hold exactly the tensors' addresses, and the marshalling helpers pass
+    such arrays through unchanged."""
+    torch = pytest.importorskip("torch")
+    import synth
+    from dense_decoder_layer_gb300.stack import DenseStack
+    dims = synth.CONFIGS["tiny"]
+    st = DenseStack(dims, 32, 8, device="cpu")
+    try:
+        assert [st._k_ptrs[i] for i in range(dims.n_layers)] == \
+            [t.data_ptr() for t in st.k_cache]
+        assert [st._v_ptrs[i] for i in range(dims.n_layers)] == \
+            [t.data_ptr() for t in st.v_cache]
+        layers = [{n: torch.empty(16, dtype=torch.bfloat16) for n in pds.LAYER_FIELDS}
+                  for _ in range(dims.n_layers)]
+        st.set_layer_tensors(layers)
+        for l, arr in zip(layers, st._layers_c):
+            for n in pds.LAYER_FIELDS:
+                assert getattr(arr, n) == l[n].data_ptr()
+        assert pds._ptrs(st._k_ptrs) is st._k_ptrs
+        assert pds._layer_array(st._layers_c) is st._layers_c
+    finally:
+        st.close()
