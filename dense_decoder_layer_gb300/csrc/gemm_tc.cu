@@ -76,6 +76,8 @@ enum EpiKind { kEpiPlain = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiQkv = 3 };
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kMinItersPerCta = 4;
+// CTAs a GEMM of a single row tile aims for (see make_schedule).
+constexpr int kSingleRowCtas = 64;
 
 struct GemmMaps {
   CUtensorMap a;
@@ -1481,12 +1483,28 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   }();
   const int ctas = std::min({c.num_sms > 0 ? c.num_sms : 148, kGemmMaxGrid, max_grid, env_cap});
   const int gmax = std::max(1, std::min(ctas / gs, g.total / kMinItersPerCta));
+  if (g.tiles_m == 1) {
+    // A single row tile streams every weight byte once and is bound by how
+    // fast the CTAs pull weights in, which wants many CTAs; but each extra
+    // CTA on a tile adds a partial tile to the finisher's serial reduction.
+    // Measured on GB300 at M = 128 (Llama-3.2-1B shapes): splits that give
+    // every tile the same number c of CTAs, c dividing the k-blocks, with
+    // about 64 CTAs in all, beat using every SM by 1.3-2.2x per GEMM.
+    int best_c = 0;
+    for (int cc = 1; g.tiles_n * cc <= ctas && cc * kMinItersPerCta <= g.kb; cc *= 2) {
+      if (g.kb % cc) continue;
+      if (!best_c || std::abs(g.tiles_n * cc - kSingleRowCtas) <
+                         std::abs(g.tiles_n * best_c - kSingleRowCtas))
+        best_c = cc;
+    }
+    g.groups = best_c ? g.tiles_n * best_c : gmax;
+    g.grid = g.groups * gs;
+    return;
+  }
   // Pick the group count by a cost model measured on GB300 for these tiles:
   // about 0.35 us per k-block of a group's range, plus, when units are split
   // across groups, about 4 us + 5 us per extra contributor for storing,
   // reducing and re-reading partial tiles.  Fewer CTAs without splits often win.
-  // A single row tile streams every weight byte once: there the bandwidth of
-  // all SMs matters more than splits, so every group is used.
   // A 128-wide tile moves two thirds of the shared-memory bytes of a 256-wide
   // one per k-block, and its k-blocks take about that much less time.
   const double kb_us = bn == 256 ? 0.35 : 0.24;
@@ -1500,7 +1518,7 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   }();
   double best = 1e30;
   int best_g = gmax;
-  for (int gr = gmax; g.tiles_m > 1 && gr >= std::max(1, gmax / 3); --gr) {
+  for (int gr = gmax; gr >= std::max(1, gmax / 3); --gr) {
     const double per = static_cast<double>(g.total) / gr;
     double cost = std::ceil(per) * kb_us;
     if (g.units % gr != 0) {
@@ -1673,7 +1691,9 @@ pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int
     const char* v = std::getenv("PDS_GEMM_BN_RESID");
     return v ? std::atoi(v) : 256;
   }();
-  const int bn = (N % 256 == 0 && env_bn != 128) ? 256 : 128;
+  // a single row tile: 128-wide tiles (twice the tiles to spread the
+  // weights over; measured faster for both residual GEMMs at M = 128)
+  const int bn = (N % 256 == 0 && env_bn != 128 && M > BM) ? 256 : 128;
   GemmArgs g{};
   g.wrows0 = N;
   g.resid = e;
