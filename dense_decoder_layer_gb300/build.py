@@ -1,8 +1,13 @@
-"""Build the in-tree CUDA library ``libpds.so`` for sm_103a with nvcc.
+"""Build the in-tree CUDA libraries for sm_103a with nvcc.
 
-Each ``csrc/*.cu`` file is compiled to an object in parallel, then linked
-into one shared library next to this file.  Objects go to ``_build/``
-(ignored by git).  Run ``python -m dense_decoder_layer_gb300.build``.
+* ``libpds.so`` (the product): every ``csrc/*.cu`` file, compiled to an
+  object in parallel and linked into one shared library next to this file.
+* ``tests/xcheck/libpds_xcheck.so`` (test-only): the independent mma.sync
+  attention kernel the GPU tests compare the product's attention against.
+  The product never loads it.
+
+Objects go to ``_build/`` (ignored by git).  Run
+``python -m dense_decoder_layer_gb300.build``.
 """
 
 from __future__ import annotations
@@ -18,6 +23,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build", "pds")
 LIB = os.path.join(HERE, "libpds.so")
+XCHECK_DIR = os.path.join(ROOT, "tests", "xcheck")
+XCHECK_LIB = os.path.join(XCHECK_DIR, "libpds_xcheck.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -28,8 +35,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+def sources(d=CSRC):
+    return sorted(os.path.join(d, f) for f in os.listdir(d) if f.endswith(".cu"))
 
 
 def _newer(target, deps):
@@ -44,16 +51,19 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(ROOT, "include", "pds.h"))
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-                    "-I" + os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
+                    "-I" + os.path.join(ROOT, "include"), "-I" + CSRC, "--expt-relaxed-constexpr"]
     if ptxas_verbose:
         flags += ["-Xptxas", "-v"]
     cc = nvcc()
-    objs, jobs = [], []
-    for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        objs.append(obj)
-        if force or _newer(obj, [src] + headers):
-            jobs.append([cc, *flags, "-c", src, "-o", obj])
+    libs = {LIB: sources(), XCHECK_LIB: sources(XCHECK_DIR)}
+    objs, jobs = {}, []
+    for lib, srcs in libs.items():
+        objs[lib] = []
+        for src in srcs:
+            obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+            objs[lib].append(obj)
+            if force or _newer(obj, [src] + headers):
+                jobs.append([cc, *flags, "-c", src, "-o", obj])
 
     def run(cmd):
         p = subprocess.run(cmd, capture_output=True, text=True)
@@ -68,11 +78,12 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
                 failed.append(cmd[-3])
     if failed:
         raise RuntimeError("nvcc failed on " + ", ".join(failed))
-    if force or jobs or _newer(LIB, objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs, "-lcudart"]
-        p = subprocess.run(cmd, capture_output=True, text=True)
-        if p.returncode:
-            raise RuntimeError("link failed:\n" + p.stdout + p.stderr)
+    for lib, lib_objs in objs.items():
+        if force or jobs or _newer(lib, lib_objs):
+            cmd = [cc, *ARCH, "-shared", "-o", lib, *lib_objs, "-lcudart"]
+            p = subprocess.run(cmd, capture_output=True, text=True)
+            if p.returncode:
+                raise RuntimeError("link failed:\n" + p.stdout + p.stderr)
     return LIB
 
 

@@ -36,8 +36,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdlib>
-#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -524,39 +522,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// Clusters of two attention CTAs that fit on the GPU at once.
-template <int HD>
-int attn_max_pairs(const cudaLaunchConfig_t& base) {
-  static std::mutex mu;
-  static int pairs = 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!pairs) {
-    cudaLaunchAttribute ca[1];
-    ca[0].id = cudaLaunchAttributeClusterDimension;
-    ca[0].val.clusterDim.x = 2;
-    ca[0].val.clusterDim.y = 1;
-    ca[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t q = base;
-    q.gridDim = dim3(2);
-    q.attrs = ca;
-    q.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<HD>, &q) != cudaSuccess || n < 1) {
-      cudaGetLastError();
-      n = 0;  // no pairs: no split
-    }
-    pairs = n;
-  }
-  return pairs;
-}
-
 template <int HD>
 pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                           uint16_t* o, int B, int s, int H, int Hkv, cudaStream_t st,
                           std::string* err) {
   using C = AttnCfg<HD>;
-  static cudaError_t attr = cudaFuncSetAttribute(
-      attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+  const void* fn = reinterpret_cast<const void*>(attn_tc_kernel<HD>);
+  const cudaError_t attr = kernel_smem_attr(fn, static_cast<int>(C::kSmem));
   if (attr != cudaSuccess) {
     *err = std::string("attention shared-memory attribute: ") + cudaGetErrorString(attr);
     return PDS_ELAUNCH;
@@ -580,7 +552,7 @@ pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, co
   // time) while every CTA still has an SM of its own: fewer tiles than SMs
   // otherwise leave SMs idle behind the longest tiles.
   const int nq = (B + kRows - 1) / kRows, tiles = H * nq;
-  const int pair_cap = std::min(c.num_sms / 2, attn_max_pairs<HD>(cfg));
+  const int pair_cap = std::min(c.num_sms / 2, kernel_max_clusters(fn, cfg, 2));
   int n_split = 0;
   for (int qt = nq - 1; qt >= 0; --qt) {
     const int nkt = (s + std::min((qt + 1) * kRows, B) + kKeys - 1) / kKeys;
@@ -621,12 +593,6 @@ pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, co
 pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
                         std::string* err) {
-  // PDS_ATTN=mma selects the warp-level mma.sync kernel (a cross-check).
-  static const bool use_mma = [] {
-    const char* e = std::getenv("PDS_ATTN");
-    return e && std::string(e) == "mma";
-  }();
-  if (use_mma) return tc_attention_mma(c, q, k, v, o, B, start_pos, H, Hkv, hd, st, err);
   return hd == 128 ? launch_attn_tc<128>(c, q, k, v, o, B, start_pos, H, Hkv, st, err)
                    : launch_attn_tc<64>(c, q, k, v, o, B, start_pos, H, Hkv, st, err);
 }

@@ -55,7 +55,9 @@
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <unordered_map>
 
 #include "sm100.cuh"
@@ -96,12 +98,13 @@ struct GemmArgs {
   // A unit is (row-tile group mg < mgs, column tile nt); the units x k-blocks
   // space (`total` iterations) is cut into `groups` equal contiguous ranges.
   int gs, mgs, units, total, groups, grid;
-  // The CTAs of a group run as clusters of cs (1, 2 or 4): each loads 1/cs
-  // of the shared weight tile and multicasts it to the whole cluster.
+  // Cluster size: 1 (every CTA loads its own tiles), 2 in pair mode, 2*split
+  // for the cluster split-K.  No load is shared between CTAs: each CTA's
+  // TMA copies fill its own shared memory only.
   int cs;
   // Pair mode (cs = 2): the two CTAs of a cluster compute a 256 x BN tile
   // with cta_group::2 MMAs, each loading its own 128 rows of A and half of
-  // the BN weight rows (no multicast).
+  // the BN weight rows.
   int pair;
   // Cluster split-K (residual GEMMs in pair mode): each cluster of 2*split
   // CTAs computes one 256 x BN tile, pair q over the q-th of `split` equal
@@ -935,9 +938,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full(s), 1);
-      // freed by the MMAs of every CTA of a multicast cluster; a pair's
-      // stages are freed by the even CTA's MMAs alone
-      mbar_init(bar_empty(s), PAIR ? 1 : g.cs);
+      // freed by this CTA's MMAs, or for a pair by the even CTA's
+      mbar_init(bar_empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull(a), 1);
@@ -974,10 +976,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // peers multicast into this CTA's stages and arrive on its barriers
+  // the peers of a pair or split cluster arrive on this CTA's barriers
   if (g.cs > 1) cluster_sync();
   const uint32_t tmem_base = misc[0];
-  const uint16_t cmask = static_cast<uint16_t>((1u << g.cs) - 1);
   // A pair (cluster ranks 2k, 2k+1): the even CTA issues the MMAs and owns
   // the stage-full and accumulator-empty barriers both CTAs' copies and
   // epilogues signal.
@@ -1007,13 +1008,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
       // A (activations) is re-read by every column tile: keep it.  A weight
-      // box is read once when one cluster holds all the row tiles of its
-      // group (it is multicast to them): let it go first; otherwise the
-      // group's other clusters read it again right away: normal priority.
+      // box is read once when one cluster (or CTA) holds all the row tiles of
+      // its group: let it go first; otherwise the group's other CTAs read it
+      // again right away: normal priority.
       const uint64_t pol_a = policy_evict_last();
       const uint64_t pol_w = g.cs == g.gs ? policy_evict_first() : policy_evict_normal();
-      const int slice = BN / g.cs;  // weight rows this CTA loads for the cluster
-      const int r0 = (g.cs > 1 && !PAIR ? static_cast<int>(cluster_rank()) : 0) * slice;
       // where a stage's copies complete: the pair leader's barrier, or our own
       auto full_bar = [&](int s) { return PAIR ? mapa_shared(bar_full(s), lead) : bar_full(s); };
       auto load_w = [&](int s, int nt, int kb) {
@@ -1023,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           b_source<BN>(g, nt, static_cast<int>(prank), mi, row);
           tma_load_2d_pair(sbase + s * C::kStage + C::kABytes, &maps.b[mi], full_bar(s), kb * BK,
                            row, pol_w);
-        } else if (g.cs == 1) {
+        } else {
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h) {
             int mi, row;
@@ -1031,11 +1030,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sbase + s * C::kStage + C::kABytes + h * 16384u, &maps.b[mi], bar_full(s),
                         kb * BK, row, pol_w);
           }
-        } else {
-          int mi, row;
-          b_source<BN>(g, nt, r0 / 128, mi, row);
-          tma_load_2d_mc(sbase + s * C::kStage + C::kABytes + r0 * 128u, &maps.b[mi], bar_full(s),
-                         kb * BK, row + (r0 % 128), cmask, pol_w);
         }
       };
       const int npre = min(S, it1 - it0);
@@ -1145,8 +1139,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if constexpr (PAIR) {
             umma_commit_pair_mc(bar_empty(s), pmask);  // the stage is free in both CTAs
-          } else if (g.cs > 1) {
-            umma_commit_mc(bar_empty(s), cmask);  // the stage is free in every CTA's view
           } else {
             umma_commit(bar_empty(s));
           }
@@ -1305,7 +1297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // no CTA leaves while a peer may still multicast into it or arrive on it
+  // no CTA leaves while a peer may still copy into it or arrive on it
   if (g.cs > 1) cluster_sync();
   if (threadIdx.x == 0) PDS_GEMM_TRACE_HOOK(cta, 6);
   if (warp == 1) {
@@ -1405,11 +1397,6 @@ pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner
   return PDS_OK;
 }
 
-// Rows of a weight box: the slice one CTA of a cluster loads.
-uint32_t weight_box_rows(const GemmArgs& g, int bn) {
-  return g.cs > 1 && !g.pair ? static_cast<uint32_t>(bn / g.cs) : 128u;
-}
-
 void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, int bn,
                    int max_grid = kGemmMaxGrid, bool allow_pair = true, int split = 0) {
   g.M = M;
@@ -1424,23 +1411,13 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   g.mgs = g.tiles_m / gs;
   g.units = g.mgs * g.tiles_n;
   g.total = g.units * g.kb;
-  // Cluster size: the largest of 4, 2 dividing the group whose weight slice is
-  // at least 64 rows.  PDS_GEMM_CLUSTER=1 turns multicast off (a tuning knob).
-  static const int env_cs = [] {
-    const char* v = std::getenv("PDS_GEMM_CLUSTER");
-    return v ? std::max(1, std::atoi(v)) : 4;
-  }();
   // Pair mode for 256-wide tiles whenever the group holds whole pairs of
   // row tiles: it halves the weight bytes each SM takes in per k-block.
-  // PDS_GEMM_PAIR=0 turns it off (a tuning knob).
-  static const bool env_pair = [] {
-    const char* v = std::getenv("PDS_GEMM_PAIR");
-    return !(v && std::atoi(v) == 0);
-  }();
+  // Otherwise every CTA runs alone (clusters of one).
   g.cs = 1;
   g.pair = 0;
   g.split = 0;
-  if (env_pair && bn == 256 && gs % 2 == 0 && allow_pair && split != 0) {
+  if (bn == 256 && gs % 2 == 0 && allow_pair && split != 0) {
     // Cluster split-K (residual epilogues only; split = 0 elsewhere): one
     // cluster of 2S CTAs per 256-row pair tile when the pair tiles alone
     // would leave at least half of the SMs idle.  split < 0 picks the
@@ -1466,22 +1443,11 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
       return;
     }
   }
-  if (env_pair && bn == 256 && gs % 2 == 0 && allow_pair) {
+  if (bn == 256 && gs % 2 == 0 && allow_pair) {
     g.pair = 1;
     g.cs = 2;
-  } else {
-    for (int cs = 4; cs >= 2; cs /= 2)
-      if (cs <= env_cs && gs % cs == 0 && bn / cs >= 64) {
-        g.cs = cs;
-        break;
-      }
   }
-  // PDS_GEMM_CTAS caps the CTAs of every GEMM (a tuning knob; default: one per SM).
-  static const int env_cap = [] {
-    const char* v = std::getenv("PDS_GEMM_CTAS");
-    return v ? std::max(1, std::atoi(v)) : 1 << 30;
-  }();
-  const int ctas = std::min({c.num_sms > 0 ? c.num_sms : 148, kGemmMaxGrid, max_grid, env_cap});
+  const int ctas = std::min({c.num_sms > 0 ? c.num_sms : 148, kGemmMaxGrid, max_grid});
   const int gmax = std::max(1, std::min(ctas / gs, g.total / kMinItersPerCta));
   if (g.tiles_m == 1) {
     // A single row tile streams every weight byte once and is bound by how
@@ -1508,14 +1474,7 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   // A 128-wide tile moves two thirds of the shared-memory bytes of a 256-wide
   // one per k-block, and its k-blocks take about that much less time.
   const double kb_us = bn == 256 ? 0.35 : 0.24;
-  // PDS_GEMM_SPLIT_US="a,b" replaces the split penalty a + b per extra
-  // contributor (a tuning knob).
-  static const std::pair<double, double> split_us = [] {
-    const char* v = std::getenv("PDS_GEMM_SPLIT_US");
-    double a = 4.0, b = 5.0;
-    if (v) std::sscanf(v, "%lf,%lf", &a, &b);
-    return std::make_pair(a, b);
-  }();
+  constexpr double kSplitUs = 4.0, kSplitPerContribUs = 5.0;
   double best = 1e30;
   int best_g = gmax;
   for (int gr = gmax; gr >= std::max(1, gmax / 3); --gr) {
@@ -1524,7 +1483,7 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
     if (g.units % gr != 0) {
       const bool aligned = g.total % gr == 0 && (g.kb % static_cast<int>(per) == 0);
       const double contrib = g.kb / per + (aligned ? 0.0 : 1.0);
-      cost += split_us.first + split_us.second * std::max(0.0, contrib - 1.0);
+      cost += kSplitUs + kSplitPerContribUs * std::max(0.0, contrib - 1.0);
     }
     if (cost < best - 1e-9) {
       best = cost;
@@ -1539,13 +1498,8 @@ template <int BN, int EPI, bool PAIR>
 pds_status launch_impl(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t st,
                        std::string* err) {
   using Cf = Cfg<BN, PAIR>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, EPI, PAIR>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(Cf::kSmem));
-  });
+  const void* fn = reinterpret_cast<const void*>(gemm_kernel<BN, EPI, PAIR>);
+  const cudaError_t attr_err = kernel_smem_attr(fn, static_cast<int>(Cf::kSmem));
   if (attr_err != cudaSuccess) {
     *err = std::string("gemm shared-memory attribute: ") + cudaGetErrorString(attr_err);
     return PDS_ELAUNCH;
@@ -1567,30 +1521,7 @@ pds_status launch_impl(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStre
   int na = 0;
   if (g.cs > 1) {
     // never more clusters than fit on the GPU at once (one CTA per SM)
-    static std::mutex mu;
-    static int max_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
-    auto fit = [&](int cs) {
-      std::lock_guard<std::mutex> lock(mu);
-      if (!max_clusters[cs]) {
-        cudaLaunchAttribute ca[1];
-        ca[0].id = cudaLaunchAttributeClusterDimension;
-        ca[0].val.clusterDim.x = cs;
-        ca[0].val.clusterDim.y = 1;
-        ca[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t q = cfg;
-        q.gridDim = dim3(cs);
-        q.attrs = ca;
-        q.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, EPI, PAIR>, &q) != cudaSuccess ||
-            n < 1) {
-          cudaGetLastError();
-          n = 1;
-        }
-        max_clusters[cs] = n;
-      }
-      return max_clusters[cs];
-    };
+    auto fit = [&](int cs) { return std::max(1, kernel_max_clusters(fn, cfg, cs)); };
     if (g.split > 1) {
       // all of a split GEMM's clusters at once, or fewer pairs per tile
       int S = g.split;
@@ -1648,6 +1579,46 @@ pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t 
 
 }  // namespace
 
+cudaError_t kernel_smem_attr(const void* fn, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, cudaError_t> done;
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return ce;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({fn, dev});
+  if (it != done.end()) return it->second;
+  ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  done[{fn, dev}] = ce;
+  return ce;
+}
+
+int kernel_max_clusters(const void* fn, const cudaLaunchConfig_t& cfg, int cs) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int>, int> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({fn, dev, cs});
+  if (it != done.end()) return it->second;
+  cudaLaunchAttribute ca[1];
+  ca[0].id = cudaLaunchAttributeClusterDimension;
+  ca[0].val.clusterDim.x = cs;
+  ca[0].val.clusterDim.y = 1;
+  ca[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t q = cfg;
+  q.gridDim = dim3(cs);
+  q.attrs = ca;
+  q.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &q) != cudaSuccess || n < 0) {
+    cudaGetLastError();
+    n = 0;
+  }
+  done[{fn, dev, cs}] = n;
+  return n;
+}
+
 pds_status tc_map_bf16(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner,
                        uint64_t outer, uint32_t box_rows, std::string* err) {
   return get_map(c, out, p, inner, outer, err, box_rows, 2);
@@ -1671,7 +1642,7 @@ pds_status tc_gemm_plain(TcContext& c, const uint16_t* A, const uint16_t* W, flo
   GemmMaps maps{};
   pds_status rc;
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, bn))) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[0], W, K, N, err)) != PDS_OK) return rc;
   maps.b[1] = maps.b[0];
   maps.b[2] = maps.b[0];
   return bn == 256 ? launch<256, kEpiPlain>(c, maps, g, st, err)
@@ -1680,29 +1651,18 @@ pds_status tc_gemm_plain(TcContext& c, const uint16_t* A, const uint16_t* W, flo
 
 pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int M, int N, int K,
                          const ResidEpilogue& e, cudaStream_t st, std::string* err) {
-  // PDS_GEMM_SPLIT caps the pairs of the cluster split-K (0 turns it off; a
-  // tuning knob).
-  static const int env_split = [] {
-    const char* v = std::getenv("PDS_GEMM_SPLIT");
-    return v ? std::atoi(v) : -1;
-  }();
-  // PDS_GEMM_BN_RESID=128 forces 128-wide tiles (a tuning knob).
-  static const int env_bn = [] {
-    const char* v = std::getenv("PDS_GEMM_BN_RESID");
-    return v ? std::atoi(v) : 256;
-  }();
   // a single row tile: 128-wide tiles (twice the tiles to spread the
   // weights over; measured faster for both residual GEMMs at M = 128)
-  const int bn = (N % 256 == 0 && env_bn != 128 && M > BM) ? 256 : 128;
+  const int bn = (N % 256 == 0 && M > BM) ? 256 : 128;
   GemmArgs g{};
   g.wrows0 = N;
   g.resid = e;
   g.resid_n = N;
-  make_schedule(g, c, M, N / bn, K, bn, kGemmMaxGrid, true, env_split);
+  make_schedule(g, c, M, N / bn, K, bn, kGemmMaxGrid, true, -1);
   GemmMaps maps{};
   pds_status rc;
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, bn))) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[0], W, K, N, err)) != PDS_OK) return rc;
   maps.b[1] = maps.b[0];
   maps.b[2] = maps.b[0];
   // residual in (whole-tile-high boxes), h and a out (one warp's 32 rows)
@@ -1725,10 +1685,9 @@ pds_status tc_gemm_swiglu(TcContext& c, const uint16_t* A, const WeightRows& W, 
   make_schedule(g, c, M, e.ffn / 128, K, 256);
   GemmMaps maps{};
   pds_status rc;
-  const uint32_t br = weight_box_rows(g, 256);
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[0], W.w[0], K, W.rows[0], err, br)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[1], W.w[1], K, W.rows[1], err, br)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[0], W.w[0], K, W.rows[0], err)) != PDS_OK) return rc;
+  if ((rc = get_map(c, &maps.b[1], W.w[1], K, W.rows[1], err)) != PDS_OK) return rc;
   maps.b[2] = maps.b[0];
   return launch<256, kEpiSwiglu>(c, maps, g, st, err);
 }
@@ -1745,10 +1704,9 @@ pds_status tc_gemm_qkv(TcContext& c, const uint16_t* A, const WeightRows& W, int
   make_schedule(g, c, M, (N + 255) / 256, K, 256);
   GemmMaps maps{};
   pds_status rc;
-  const uint32_t br = weight_box_rows(g, 256);
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
   for (int i = 0; i < 3; ++i)
-    if ((rc = get_map(c, &maps.b[i], W.w[i], K, W.rows[i], err, br)) != PDS_OK) return rc;
+    if ((rc = get_map(c, &maps.b[i], W.w[i], K, W.rows[i], err)) != PDS_OK) return rc;
   return launch<256, kEpiQkv>(c, maps, g, st, err);
 }
 
@@ -1804,6 +1762,25 @@ pds_status noalloc_scratch(char** out, std::string* err) {
 
 size_t tc_gemm_noalloc_max_tiles() { return kNoAllocCounterBytes / 4; }
 
+pds_status tc_noalloc_take_status(uint32_t* flags, std::string* err) {
+  *flags = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return PDS_OK;
+  char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    base = g_noalloc_addr[dev];
+  }
+  if (!base) return PDS_OK;  // no call on this device yet
+  cudaError_t ce = cudaMemcpy(flags, base, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (ce == cudaSuccess && *flags) ce = cudaMemset(base, 0, sizeof(uint32_t));
+  if (ce != cudaSuccess) {
+    *err = std::string("static scratch status word: ") + cudaGetErrorString(ce);
+    return PDS_ELAUNCH;
+  }
+  return PDS_OK;
+}
+
 pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Cout, int M, int N,
                                  int K, int num_sms, cudaStream_t st, std::string* err) {
   const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * (N / kNoAllocBN);
@@ -1824,6 +1801,8 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
       (kNoAllocScratchBytes - kNoAllocStatusBytes - kNoAllocCounterBytes) / per_cta);
 
   // The counters are shared with earlier calls: they must start at zero.
+  // The status word keeps what earlier calls set until pds_component_sync
+  // reads and clears it.
   cudaError_t ce = cudaMemsetAsync(counters, 0, tiles * 4, st);
   if (ce != cudaSuccess) {
     *err = std::string("static scratch counter reset: ") + cudaGetErrorString(ce);
@@ -1839,8 +1818,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   g.cs = 1;  // a plain launch, without clusters
   GemmMaps maps{};
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
-  if ((rc = get_map(c, &maps.b[0], W, K, N, err, weight_box_rows(g, kNoAllocBN))) != PDS_OK)
-    return rc;
+  if ((rc = get_map(c, &maps.b[0], W, K, N, err)) != PDS_OK) return rc;
   maps.b[1] = maps.b[0];
   maps.b[2] = maps.b[0];
   g.status = status;
@@ -1848,13 +1826,9 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   g.counters = counters;
 
   using Cf = Cfg<kNoAllocBN, false>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<kNoAllocBN, kEpiPlain, false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(Cf::kSmem));
-  });
+  const cudaError_t attr_err =
+      kernel_smem_attr(reinterpret_cast<const void*>(gemm_kernel<kNoAllocBN, kEpiPlain, false>),
+                       static_cast<int>(Cf::kSmem));
   if (attr_err != cudaSuccess) {
     *err = std::string("gemm shared-memory attribute: ") + cudaGetErrorString(attr_err);
     return PDS_ELAUNCH;

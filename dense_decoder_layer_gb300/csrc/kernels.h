@@ -14,7 +14,7 @@ struct WeightRows {
   int n;  // number of blocks in use
 };
 
-// ---- epilogue descriptions (shared by the naive and tensor-core paths) ----
+// ---- epilogue descriptions of the tensor-core GEMMs ----
 
 // RMSNorm row scale from sum-of-squares partials [M, ss_parts], one per
 // 64-column group of the row.
@@ -58,25 +58,23 @@ struct SwigluEpilogue {
 
 // ---------------------------------------------------------------- launches
 
-// (cos, sin) of pos*omega_i for pos = start_pos + b, b < M, i < hd/2, laid
-// out [i][b] (table[i * M + b]).
-void launch_rope_table(float2* table, int M, int start_pos, int half, double theta,
-                       int head_dim, cudaStream_t st);
+// Angular frequencies of the rotated pairs and the scale of the rotated
+// channels: pair i of a head turns by p * omega[i] at position p, and
+// cos/sin are multiplied by mscale.  omega is formed on the host in
+// float64.
+constexpr int kMaxRopePairs = 64;
+struct RopeFreqs {
+  double omega[kMaxRopePairs];
+  int n_pairs;  // rot_dim / 2
+  float mscale;
+};
 
-// First-layer norm prep: a = bf16(x * gain), ss partials.
+// (cos, sin) * mscale of p*omega_i for p = start_pos + b, b < M, i < n_pairs,
+// laid out [i][b] (table[i * M + b]).
+void launch_rope_table(float2* table, int M, int start_pos, const RopeFreqs& f, cudaStream_t st);
+
+// First-layer norm prep: a = bf16(x * gain), ss partials [M, d/64].
 void launch_norm_prep(const float* x, const float* gain, uint16_t* a_out, float* ss_out, int M,
                       int d, cudaStream_t st);
-
-// Naive (SIMT) path: C = A . W^T into float32, then separate epilogues.
-void launch_gemm_naive(const uint16_t* A, const WeightRows& W, float* C, int M, int N, int K,
-                       cudaStream_t st);
-void launch_qkv_epilogue_naive(const float* C, const QkvEpilogue& e, int M, cudaStream_t st);
-void launch_resid_epilogue_naive(const float* C, const ResidEpilogue& e, int M, int N,
-                                 cudaStream_t st);
-void launch_swiglu_epilogue_naive(const float* C, const SwigluEpilogue& e, int M,
-                                  cudaStream_t st);
-void launch_attention_naive(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                            uint16_t* o, int B, int start_pos, int H, int Hkv, int hd,
-                            cudaStream_t st);
 
 }  // namespace pds

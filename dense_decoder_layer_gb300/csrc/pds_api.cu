@@ -74,20 +74,13 @@ Layout make_layout(const Plan& p, int B) {
   L.o = take(Bz * p.q_width * 2);
   L.act = take(Bz * p.dims.ffn_dim * 2);
   L.rope = take(Bz * (p.dims.head_dim / 2) * 8);
-  if (p.impl == Impl::kNaive) {
-    size_t n = std::max<size_t>({(size_t)p.q_width + 2 * p.kv_width,
-                                 2 * (size_t)p.dims.ffn_dim, (size_t)d});
-    L.c32 = take(Bz * n * 4);
-  } else {
-    L.gemm_ws = take(gemm_workspace_bytes(p, B));
-  }
+  L.gemm_ws = take(gemm_workspace_bytes(p, B));
   L.total = off;
   return L;
 }
 
 }  // namespace pds
 
-using pds::Impl;
 using pds::Plan;
 
 struct pds_plan : Plan {};
@@ -121,12 +114,21 @@ pds_status pds_plan_create(const pds_dims* dims, pds_plan** out) {
   p->dims = d;
   p->q_width = d.n_heads * d.head_dim;
   p->kv_width = d.n_kv_heads * d.head_dim;
-  const char* impl = std::getenv("PDS_KERNELS");
-  p->impl = (impl && std::strcmp(impl, "naive") == 0) ? Impl::kNaive : Impl::kTensorCore;
   const char* g = std::getenv("PDS_GRAPH");
   p->graphs = !(g && std::strcmp(g, "0") == 0);
-  const char* pdl = std::getenv("PDS_PDL");
-  p->pdl = !(pdl && std::strcmp(pdl, "0") == 0);
+  // The plan's device state, on the current device, once the shape is
+  // admitted; without a CUDA device the plan stays host-only.
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+    std::string err;
+    const pds_status st = pds::plan_attach_device(*p, &err);
+    if (st != PDS_OK) {
+      delete p;
+      return fail(st, err);
+    }
+  } else {
+    cudaGetLastError();
+  }
   *out = p;
   return PDS_OK;
 }
@@ -231,8 +233,19 @@ pds_status pds_selftest_stuck_wait(uint32_t limit_us, void* stream) {
     return fail(PDS_EINVAL, "pds_selftest_stuck_wait: limit_us must be in (0, 10 s]");
   std::string err;
   pds_status st = pds::run_stuck_wait(limit_us, static_cast<cudaStream_t>(stream), &err);
-  t_last_error = err;  // an ETIMEOUT here is the expected outcome, not a failure to report
-  return st;
+  if (st != PDS_OK) return fail(st, err);
+  return PDS_OK;
+}
+
+pds_status pds_component_sync(void* stream) {
+  std::string err;
+  pds_status st = pds::component_sync(static_cast<cudaStream_t>(stream), &err);
+  if (st == PDS_ETIMEOUT) {
+    t_last_error = err;  // reported to the caller, who asked for it
+    return st;
+  }
+  if (st != PDS_OK) return fail(st, err);
+  return PDS_OK;
 }
 
 pds_status pds_plan_set_timing(pds_plan* plan, int32_t enable) {

@@ -14,13 +14,11 @@ namespace pds {
 
 struct TmapCache;
 
-enum class Impl { kTensorCore, kNaive };
-
 struct Plan {
   pds_dims dims{};
   int q_width = 0, kv_width = 0;
-  Impl impl = Impl::kTensorCore;
-  // Device state made on first use (the device current at that time).
+  // Device state made by pds_plan_create on the device current then (none
+  // when the plan was made without a CUDA device).
   int device = -1;
   int num_sms = 0;
   uint32_t* d_status = nullptr;  // status word written by bounded device waits
@@ -38,9 +36,10 @@ struct Plan {
   double total_ms[PDS_KERNEL_KINDS] = {};
   // CUDA graphs of recent call shapes: the whole call (every kernel of every
   // layer) is captured once per key (all pointers, start_pos, batch) and
-  // replayed.  PDS_GRAPH=0 turns this off.
+  // replayed; at most kMaxGraphs are kept (least recently used goes).
+  // PDS_GRAPH=0 turns this off (every call is enqueued kernel by kernel).
+  static constexpr size_t kMaxGraphs = 4;
   bool graphs = true;
-  bool pdl = true;  // programmatic dependent launch between GEMMs (PDS_PDL=0 off)
   struct Graph {
     std::vector<uintptr_t> key;
     cudaGraphExec_t exec = nullptr;
@@ -53,7 +52,7 @@ struct Plan {
 
 // Byte offsets into the caller's workspace.
 struct Layout {
-  size_t x, h, a, ss_attn, ss_ffn, q, o, act, rope, c32, gemm_ws, total;
+  size_t x, h, a, ss_attn, ss_ffn, q, o, act, rope, gemm_ws, total;
 };
 
 Layout make_layout(const Plan& p, int B);
@@ -71,6 +70,8 @@ pds_status run_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
                      uint16_t* const* v_cache, int start_pos, int B, const float* x_in,
                      float* x_out, char* ws, cudaStream_t st, std::string* err);
 
+// Make the plan's device state on the current device (pds_plan_create).
+pds_status plan_attach_device(Plan& p, std::string* err);
 pds_status plan_sync(Plan& p, cudaStream_t st, std::string* err);
 pds_status plan_kernel_times(Plan& p, cudaStream_t st, pds_kernel_times* out, bool reset,
                              std::string* err);
@@ -79,6 +80,11 @@ void plan_release_device(Plan& p);
 pds_status run_gemm_plain(const uint16_t* A, const uint16_t* W, float* C, int M, int N, int K,
                           char* ws, size_t ws_bytes, cudaStream_t st, std::string* err);
 pds_status run_stuck_wait(uint32_t limit_us, cudaStream_t st, std::string* err);
+// Synchronize and take (read and clear) the status words of the component
+// entry points on the current device.
+pds_status component_sync(cudaStream_t st, std::string* err);
+// Address of the component entry points' status word on the current device.
+uint32_t* component_status(std::string* err);
 pds_status run_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
                          int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
                          std::string* err);

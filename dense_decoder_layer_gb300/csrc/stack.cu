@@ -35,37 +35,38 @@ pds_status check_launch(const char* what, std::string* err) {
   return PDS_OK;
 }
 
-pds_status ensure_device_state(Plan& p, std::string* err) {
+// The plan's device state, made on the current device by pds_plan_create;
+// every call must run with that device current.
+pds_status check_device_state(const Plan& p, std::string* err) {
+  if (!p.d_status) {
+    *err = "the plan has no device state (it was created without a CUDA device)";
+    return PDS_ELAUNCH;
+  }
   int dev = -1;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) {
     *err = std::string("no CUDA device: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;
   }
-  if (p.d_status && p.device == dev) return PDS_OK;
-  if (p.d_status) {
-    *err = "plan used on a second device";
+  if (dev != p.device) {
+    *err = "plan used on device " + std::to_string(dev) + ", created on device " +
+           std::to_string(p.device);
     return PDS_EINVAL;
   }
-  ce = cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, dev);
-  if (ce == cudaSuccess) ce = cudaMalloc(&p.d_status, sizeof(uint32_t));
-  if (ce == cudaSuccess) ce = cudaMemset(p.d_status, 0, sizeof(uint32_t));
-  if (ce == cudaSuccess) ce = cudaMallocHost(&p.h_status, sizeof(uint32_t));
-  if (ce != cudaSuccess) {
-    *err = std::string("plan device state: ") + cudaGetErrorString(ce);
-    if (p.d_status) cudaFree(p.d_status);
-    p.d_status = nullptr;
-    p.h_status = nullptr;
-    return PDS_ENOMEM;
-  }
-  *p.h_status = 0;
-  p.device = dev;
-  if (!p.maps) p.maps = tmap_cache_create();
   return PDS_OK;
 }
 
 // Status word of the component entry points (no plan).
 __device__ uint32_t g_component_status;
+
+int current_num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
 
 uint32_t* component_status(std::string* err) {
   void* p = nullptr;
@@ -77,14 +78,57 @@ uint32_t* component_status(std::string* err) {
   return static_cast<uint32_t*>(p);
 }
 
-int current_num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
+pds_status component_sync(cudaStream_t st, std::string* err) {
+  cudaError_t ce = cudaStreamSynchronize(st);
+  if (ce != cudaSuccess) {
+    *err = std::string("stream synchronize: ") + cudaGetErrorString(ce);
+    return PDS_ELAUNCH;
+  }
+  uint32_t flags = 0;
+  ce = cudaMemcpyFromSymbol(&flags, g_component_status, sizeof(flags));
+  if (ce == cudaSuccess && flags) {
+    const uint32_t zero = 0;
+    ce = cudaMemcpyToSymbol(g_component_status, &zero, sizeof(zero));
+  }
+  if (ce != cudaSuccess) {
+    *err = std::string("component status word: ") + cudaGetErrorString(ce);
+    return PDS_ELAUNCH;
+  }
+  uint32_t noalloc_flags = 0;
+  pds_status rc = tc_noalloc_take_status(&noalloc_flags, err);
+  if (rc != PDS_OK) return rc;
+  flags |= noalloc_flags;
+  if (flags & kStatusTimeout) {
+    *err = "a bounded device wait of a component call gave up (status word " +
+           std::to_string(flags) + ")";
+    return PDS_ETIMEOUT;
+  }
+  if (flags) {
+    *err = "component status word " + std::to_string(flags);
+    return PDS_ELAUNCH;
+  }
+  return PDS_OK;
 }
 
-}  // namespace
+pds_status plan_attach_device(Plan& p, std::string* err) {
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess)
+    ce = cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce == cudaSuccess) ce = cudaMalloc(&p.d_status, sizeof(uint32_t));
+  if (ce == cudaSuccess) ce = cudaMemset(p.d_status, 0, sizeof(uint32_t));
+  if (ce == cudaSuccess) ce = cudaMallocHost(&p.h_status, sizeof(uint32_t));
+  if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&p.capture_stream, cudaStreamNonBlocking);
+  if (ce != cudaSuccess) {
+    *err = std::string("plan device state: ") + cudaGetErrorString(ce);
+    plan_release_device(p);
+    return PDS_ENOMEM;
+  }
+  *p.h_status = 0;
+  p.device = dev;
+  p.maps = tmap_cache_create();
+  return PDS_OK;
+}
 
 size_t gemm_workspace_bytes(const Plan& p, int B) {
   const int n_qkv = p.q_width + 2 * p.kv_width;
@@ -148,7 +192,7 @@ pds_status plan_sync(Plan& p, cudaStream_t st, std::string* err) {
 pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
                          uint16_t* const* v_cache, int s, int B, const float* x_in, float* x_out,
                          char* ws, cudaStream_t st, std::string* err) {
-  pds_status rc = ensure_device_state(p, err);
+  pds_status rc = check_device_state(p, err);
   if (rc != PDS_OK) return rc;
   const pds_dims& D = p.dims;
   const int d = D.d_model, F = D.ffn_dim, hd = D.head_dim, L = D.n_layers;
@@ -185,20 +229,28 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
     if (m) cudaEventRecord(m->stop, st);
   };
 
+  // RoPE frequencies in float64: omega_i = theta^(-2i/hd) (cuda_prefill.rs,
+  // LayerRopeCuda: theta, rot_dim = head_dim)
+  RopeFreqs rf{};
+  rf.n_pairs = hd / 2;
+  rf.mscale = 1.0f;
+  for (int i = 0; i < rf.n_pairs; ++i)
+    rf.omega[i] = std::pow(static_cast<double>(D.rope_theta), -2.0 * i / hd);
+
   Plan::Mark* mk = mark(PDS_KERNEL_PREP);
-  launch_rope_table(rope, B, s, hd / 2, (double)D.rope_theta, hd, st);
+  launch_rope_table(rope, B, s, rf, st);
   launch_norm_prep(x_in, layers[0].attn_norm_w, A, ss_attn, B, d, st);
   done(mk);
   if ((rc = check_launch("norm prep", err)) != PDS_OK) return rc;
 
   TcContext tc{};
-  if (p.impl == Impl::kTensorCore) {
-    tc.num_sms = p.num_sms;
-    tc.status = p.d_status;
-    tc.ws = ws + lay.gemm_ws;
-    tc.ws_bytes = gemm_workspace_bytes(p, B);
-    tc.maps = p.maps;
-    tc.pdl = p.pdl;
+  tc.num_sms = p.num_sms;
+  tc.status = p.d_status;
+  tc.ws = ws + lay.gemm_ws;
+  tc.ws_bytes = gemm_workspace_bytes(p, B);
+  tc.maps = p.maps;
+  tc.pdl = true;
+  {
     // stream-K tile counters start at zero; every GEMM leaves them at zero
     const size_t part = tc_gemm_scratch_bytes(B, 0);
     cudaError_t ce = cudaMemsetAsync(tc.ws + part, 0, tc.ws_bytes - part, st);
@@ -230,56 +282,29 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
     ResidEpilogue oe{x_cur, Hs, w.ffn_norm_w, A, ss_ffn};
     SwigluEpilogue ge{RowScale{ss_ffn, parts, inv_d, D.rms_eps}, ACT, F};
     WeightRows wgu{{w.w_gate, w.w_up, nullptr}, {F, F, 0}, 2};
-    WeightRows wo{{w.wo, nullptr, nullptr}, {d, 0, 0}, 1};
-    WeightRows wd{{w.w_down, nullptr, nullptr}, {d, 0, 0}, 1};
     ResidEpilogue de{Hs, x_next, g_next, A, ss_attn};
 
-    if (p.impl == Impl::kNaive) {
-      float* C = reinterpret_cast<float*>(ws + lay.c32);
-      const int nqkv = p.q_width + 2 * p.kv_width;
-      mk = mark(PDS_KERNEL_QKV);
-      launch_gemm_naive(A, wqkv, C, B, nqkv, d, st);
-      launch_qkv_epilogue_naive(C, qe, B, st);
-      done(mk);
-      mk = mark(PDS_KERNEL_ATTN);
-      launch_attention_naive(Q, k_cache[l], v_cache[l], O, B, s, D.n_heads, D.n_kv_heads, hd, st);
-      done(mk);
-      mk = mark(PDS_KERNEL_WO);
-      launch_gemm_naive(O, wo, C, B, d, p.q_width, st);
-      launch_resid_epilogue_naive(C, oe, B, d, st);
-      done(mk);
-      mk = mark(PDS_KERNEL_GATEUP);
-      launch_gemm_naive(A, wgu, C, B, 2 * F, d, st);
-      launch_swiglu_epilogue_naive(C, ge, B, st);
-      done(mk);
-      mk = mark(PDS_KERNEL_DOWN);
-      launch_gemm_naive(ACT, wd, C, B, d, F, st);
-      launch_resid_epilogue_naive(C, de, B, d, st);
-      done(mk);
-      if ((rc = check_launch("naive layer", err)) != PDS_OK) return rc;
-    } else {
-      mk = mark(PDS_KERNEL_QKV);
-      rc = tc_gemm_qkv(tc, A, wqkv, B, d, qe, st, err);
-      done(mk);
-      if (rc != PDS_OK) return rc;
-      mk = mark(PDS_KERNEL_ATTN);
-      rc = tc_attention(tc, Q, k_cache[l], v_cache[l], O, B, s, D.n_heads, D.n_kv_heads, hd, st,
-                        err);
-      done(mk);
-      if (rc != PDS_OK) return rc;
-      mk = mark(PDS_KERNEL_WO);
-      rc = tc_gemm_resid(tc, O, w.wo, B, d, p.q_width, oe, st, err);
-      done(mk);
-      if (rc != PDS_OK) return rc;
-      mk = mark(PDS_KERNEL_GATEUP);
-      rc = tc_gemm_swiglu(tc, A, wgu, B, d, ge, st, err);
-      done(mk);
-      if (rc != PDS_OK) return rc;
-      mk = mark(PDS_KERNEL_DOWN);
-      rc = tc_gemm_resid(tc, ACT, w.w_down, B, d, F, de, st, err);
-      done(mk);
-      if (rc != PDS_OK) return rc;
-    }
+    mk = mark(PDS_KERNEL_QKV);
+    rc = tc_gemm_qkv(tc, A, wqkv, B, d, qe, st, err);
+    done(mk);
+    if (rc != PDS_OK) return rc;
+    mk = mark(PDS_KERNEL_ATTN);
+    rc = tc_attention(tc, Q, k_cache[l], v_cache[l], O, B, s, D.n_heads, D.n_kv_heads, hd, st,
+                      err);
+    done(mk);
+    if (rc != PDS_OK) return rc;
+    mk = mark(PDS_KERNEL_WO);
+    rc = tc_gemm_resid(tc, O, w.wo, B, d, p.q_width, oe, st, err);
+    done(mk);
+    if (rc != PDS_OK) return rc;
+    mk = mark(PDS_KERNEL_GATEUP);
+    rc = tc_gemm_swiglu(tc, A, wgu, B, d, ge, st, err);
+    done(mk);
+    if (rc != PDS_OK) return rc;
+    mk = mark(PDS_KERNEL_DOWN);
+    rc = tc_gemm_resid(tc, ACT, w.w_down, B, d, F, de, st, err);
+    done(mk);
+    if (rc != PDS_OK) return rc;
   }
   return PDS_OK;
 }
@@ -289,7 +314,7 @@ pds_status run_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
                      char* ws, cudaStream_t st, std::string* err) {
   if (!p.graphs || p.timing)
     return enqueue_stack(p, layers, k_cache, v_cache, s, B, x_in, x_out, ws, st, err);
-  pds_status rc = ensure_device_state(p, err);
+  pds_status rc = check_device_state(p, err);
   if (rc != PDS_OK) return rc;
   std::vector<uintptr_t> key;
   key.reserve(8 + 11 * p.dims.n_layers);
@@ -310,10 +335,7 @@ pds_status run_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
   for (Plan::Graph& g : p.graph_cache)
     if (g.key == key) hit = &g;
   if (!hit) {
-    cudaError_t ce = cudaSuccess;
-    if (!p.capture_stream) ce = cudaStreamCreateWithFlags(&p.capture_stream, cudaStreamNonBlocking);
-    if (ce == cudaSuccess)
-      ce = cudaStreamBeginCapture(p.capture_stream, cudaStreamCaptureModeRelaxed);
+    cudaError_t ce = cudaStreamBeginCapture(p.capture_stream, cudaStreamCaptureModeRelaxed);
     if (ce != cudaSuccess) {
       *err = std::string("graph capture start: ") + cudaGetErrorString(ce);
       return PDS_ELAUNCH;
@@ -337,8 +359,7 @@ pds_status run_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
       *err = std::string("graph instantiate: ") + cudaGetErrorString(ce);
       return PDS_ELAUNCH;
     }
-    constexpr size_t kMaxGraphs = 4;
-    if (p.graph_cache.size() >= kMaxGraphs) {
+    if (p.graph_cache.size() >= Plan::kMaxGraphs) {
       auto lru = std::min_element(p.graph_cache.begin(), p.graph_cache.end(),
                                   [](const Plan::Graph& a, const Plan::Graph& b) {
                                     return a.last_use < b.last_use;

@@ -46,17 +46,23 @@ pds_status tc_gemm_swiglu(TcContext& c, const uint16_t* A, const WeightRows& W, 
 // caller buffer (allocates nothing); at most tc_gemm_noalloc_max_tiles()
 // output tiles of 128 x 128.
 size_t tc_gemm_noalloc_max_tiles();
+// Read and clear the status word of the current device's static scratch
+// (0 if the no-allocation GEMM has not run on this device).
+pds_status tc_noalloc_take_status(uint32_t* flags, std::string* err);
 pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* C, int M, int N,
                                  int K, int num_sms, cudaStream_t st, std::string* err);
 // Tensor map of a row-major bf16 matrix [outer, inner]: boxes of 64 columns
 // (128 bytes, 128-byte swizzle) x box_rows rows; cached in c.maps.
+// Launch facts of a kernel on the current device, made once per (kernel,
+// device) with that device current (function attributes and occupancy are
+// per device): the dynamic shared-memory limit of `fn`, and how many
+// clusters of `cs` CTAs of `fn` launched with `cfg` fit on the GPU at once
+// (0 if the query fails).
+cudaError_t kernel_smem_attr(const void* fn, int bytes);
+int kernel_max_clusters(const void* fn, const cudaLaunchConfig_t& cfg, int cs);
 pds_status tc_map_bf16(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner,
                        uint64_t outer, uint32_t box_rows, std::string* err);
-// GQA causal attention: the tcgen05 kernel (head_dim 64 or 128), or the
-// warp-level mma.sync kernel when PDS_ATTN=mma.
-pds_status tc_attention_mma(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                            uint16_t* o, int B, int start_pos, int H, int Hkv, int hd,
-                            cudaStream_t st, std::string* err);
+// GQA causal attention on the tcgen05 tensor cores (head_dim 64 or 128).
 pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
                         std::string* err);

@@ -83,6 +83,7 @@ def load() -> ctypes.CDLL:
         "pds_attention": (st, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "pds_plan_set_timing": (st, [vp, i32]),
         "pds_selftest_stuck_wait": (st, [ctypes.c_uint32, vp]),
+        "pds_component_sync": (st, [vp]),
         "pds_plan_kernel_times": (st, [vp, vp, ctypes.POINTER(pds_kernel_times), i32]),
     }
     for name, (res, args) in sig.items():
@@ -197,6 +198,15 @@ def pds_plan_kernel_times(plan, stream, reset: bool = False) -> dict:
     return {k: (kt.launches[i], kt.total_ms[i]) for i, k in enumerate(KERNEL_KINDS)}
 
 
-def pds_selftest_stuck_wait(limit_us: int, stream) -> int:
-    """Status of the bounded-wait self test (PDS_ETIMEOUT is the expected answer)."""
-    return load().pds_selftest_stuck_wait(limit_us, stream)
+def pds_selftest_stuck_wait(limit_us: int, stream) -> None:
+    """Enqueue the bounded-wait self test (its timeout shows in pds_component_sync)."""
+    check(load().pds_selftest_stuck_wait(limit_us, stream))
+
+
+def pds_component_sync(stream) -> int:
+    """Status of the component calls since the last sync (PDS_OK or PDS_ETIMEOUT);
+    other failures raise."""
+    st = load().pds_component_sync(stream)
+    if st not in (PDS_OK, PDS_ETIMEOUT):
+        raise PdsError(st, last_error())
+    return st

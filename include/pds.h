@@ -92,16 +92,34 @@ typedef struct pds_layer {
 typedef struct pds_plan pds_plan;
 
 /*
- * Validate the dimensions and make a plan.  Host only: touches no GPU.
- * Returns PDS_DECLINED (with *out = NULL) for shapes the kernels do not
- * serve (see the field comments of pds_dims) or when the environment
- * variable PDS_DISABLE is set to a non-empty value other than "0"
- * (cuda_prefill.rs: the cuda_dense_enabled() switch); PDS_EINVAL for a
- * NULL argument or a non-positive size.  Destroy with pds_plan_destroy.
+ * Validate the dimensions and make a plan.
+ *
+ * Validation is host-only and comes first: PDS_DECLINED (with *out = NULL)
+ * for shapes the kernels do not serve (see the field comments of pds_dims)
+ * or when the environment variable PDS_DISABLE is set to a non-empty value
+ * other than "0" (cuda_prefill.rs: the cuda_dense_enabled() switch), and
+ * PDS_EINVAL for a NULL argument or a non-positive size, are decided before
+ * any device work.
+ *
+ * An admitted plan then makes all the device state the library itself
+ * allocates, on the device current at this call, which the plan is bound
+ * to: a 4-byte status word (cudaMalloc), its 4-byte pinned host copy
+ * (cudaMallocHost) and a non-blocking capture stream; PDS_ENOMEM if that
+ * fails.  No later call allocates device memory, except that instantiating
+ * a CUDA graph of a call (see pds_prefill_dense_stack_device) makes the
+ * driver hold memory for its executable graph: at most four per plan, each
+ * of 2 + 5 * n_layers kernel nodes, freed by pds_plan_destroy.  Without a
+ * CUDA device the plan is host-only: validation and pds_workspace_bytes
+ * work, and every call returns PDS_ELAUNCH.
+ *
+ * Weights are used in place: the kernels read the caller's row-major
+ * [out, in] bf16 matrices through TMA tensor maps built at call time
+ * (128-byte swizzled boxes straight from the caller's layout), so there is
+ * no packing step and no packed copy of the weights.
  */
 pds_status pds_plan_create(const pds_dims* dims, pds_plan** out);
 
-/* Release a plan and the small device state it made on first use. NULL is a no-op. */
+/* Release a plan, its device state and its graphs. NULL is a no-op. */
 void pds_plan_destroy(pds_plan* plan);
 
 /*
@@ -147,6 +165,13 @@ pds_status pds_prefill_dense_stack(pds_plan* plan, const pds_layer* layers,
  * The same call with device input and output (float32 [B, d] each, may
  * alias), enqueued on the stream without synchronizing.  A device-side
  * timeout is reported by the next pds_plan_sync (or host-I/O call).
+ *
+ * Launch mode: the first call with a given set of pointers, start_pos and
+ * batch captures all of the call's kernels into a CUDA graph, later calls
+ * with the same set replay it (four sets are kept per plan, the least
+ * recently used is dropped).  A caller whose pointers change on every call
+ * can set the environment variable PDS_GRAPH=0 before pds_plan_create to
+ * enqueue the kernels one by one instead; the computation is the same.
  */
 pds_status pds_prefill_dense_stack_device(pds_plan* plan, const pds_layer* layers,
                                           uint16_t* const* k_cache, uint16_t* const* v_cache,
@@ -189,12 +214,14 @@ typedef struct pds_kernel_times {
 } pds_kernel_times;
 
 /*
- * Failure-detection self test (no counterpart on the pages).  Runs a
- * one-CTA kernel that waits on an mbarrier nothing ever arrives on, through
- * the same bounded wait every tensor-core kernel of the library uses, with
- * a limit of limit_us microseconds.  Returns PDS_ETIMEOUT when the wait gave
- * up, set the timeout bit and let the kernel exit (the expected outcome),
- * PDS_OK if the wait somehow completed.  Synchronizes the stream.
+ * Failure-detection self test (no counterpart on the pages), a component
+ * entry point like the ones below: enqueues on the stream a one-CTA kernel
+ * that waits on an mbarrier nothing ever arrives on, through the same
+ * bounded wait every tensor-core kernel of the library uses, with a limit of
+ * limit_us microseconds (0 < limit_us <= 10 s, else PDS_EINVAL).  The wait
+ * gives up, sets the timeout bit of the component status word and the
+ * kernel exits; the next pds_component_sync returns PDS_ETIMEOUT.  Returns
+ * PDS_OK once enqueued.
  */
 pds_status pds_selftest_stuck_wait(uint32_t limit_us, void* stream);
 
@@ -205,8 +232,21 @@ pds_status pds_plan_kernel_times(pds_plan* plan, void* stream, pds_kernel_times*
 /*
  * Component entry points: the stack's kernels one at a time, on device
  * buffers, enqueued on the stream (no synchronization).  They serve the
- * kernel-level tests and take the same shape limits as the stack.
+ * kernel-level tests and take the same shape limits as the stack.  Their
+ * kernels' bounded waits report a timeout in a status word of the library
+ * (one per device), which pds_component_sync reads.
  */
+
+/*
+ * Synchronize the stream, then read and clear the component status words
+ * of the current device (those of pds_gemm_bf16, pds_gemm_bf16_noalloc,
+ * pds_attention and pds_selftest_stuck_wait).  Returns PDS_ETIMEOUT if a
+ * bounded device wait of any of their kernels gave up since the previous
+ * pds_component_sync on this device (the output of that call is then not
+ * valid), PDS_ELAUNCH if the stream reports a CUDA error, else PDS_OK.
+ * Allocates nothing.
+ */
+pds_status pds_component_sync(void* stream);
 
 /*
  * C[M, N] (float32, row-major, ldc = N) = A[M, K] . W[N, K]^T for bf16 A and
@@ -243,7 +283,8 @@ size_t pds_gemm_workspace_bytes(int32_t M, int32_t N);
  * on the same GPU, on any streams, race -- order them on one stream or
  * serialize them.  The first call on a device looks up the array's device
  * address for that device (set-up); make that first call before any
- * stream capture.
+ * stream capture.  A device-side timeout of the call is reported by
+ * pds_component_sync, which reads and clears the array's status word.
  */
 pds_status pds_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* W, float* C, int32_t M,
                                  int32_t N, int32_t K, void* stream);

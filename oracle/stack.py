@@ -21,7 +21,7 @@ Sources (frink-models pages):
   ``device_attention_layer``: q/k/v reach attention post-RoPE, the layer
   ends with ``wo``, the residual, the FFN norm, the FFN and the residual.
 
-Readings where the pages are silent (all listed in the design doc):
+Readings where the pages are silent:
 weights are ``[out, in]`` and ``y = x @ W.T``; RoPE is the NeoX-half
 layout with ``omega_i = theta**(-2i/head_dim)`` over the full head;
 query head ``h`` reads kv head ``h // (n_heads/n_kv_heads)``; new row

@@ -3,7 +3,6 @@
 from __future__ import annotations
 
 import functools
-import os
 
 import numpy as np
 
@@ -66,19 +65,11 @@ def oracle_result(name_or_dims, seed=0, rows=None):
     return run_oracle(dims, layers, pk, pv, hidden)
 
 
-def run_gpu(dims, layers, pk, pv, hidden, impl="tc", extra_capacity=0):
+def run_gpu(dims, layers, pk, pv, hidden, extra_capacity=0):
     """One host-I/O call of the CUDA stack; returns (hidden_out, [k], [v]) as float64."""
     import torch
     from dense_decoder_layer_gb300.stack import DenseStack
-    old = os.environ.get("PDS_KERNELS")
-    os.environ["PDS_KERNELS"] = "naive" if impl == "naive" else "tc"
-    try:
-        st = DenseStack(dims, dims.start_pos + dims.batch + extra_capacity, dims.batch)
-    finally:
-        if old is None:
-            os.environ.pop("PDS_KERNELS", None)
-        else:
-            os.environ["PDS_KERNELS"] = old
+    st = DenseStack(dims, dims.start_pos + dims.batch + extra_capacity, dims.batch)
     st.load_layers(layers)
     st.load_prefix(pk, pv)
     out = st.prefill(torch.from_numpy(np.ascontiguousarray(hidden, np.float32)), dims.start_pos)

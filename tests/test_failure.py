@@ -51,11 +51,15 @@ def test_selftest_rejects_bad_limits():
 
 @pytest.mark.gpu
 def test_stuck_device_wait_times_out_and_gpu_stays_usable():
+    """The component path reports a bounded wait that gave up, clears it, and
+    the context stays usable: a GEMM right after runs and is right."""
     torch = pytest.importorskip("torch")
     stream = torch.cuda.current_stream().cuda_stream
-    assert pds.pds_selftest_stuck_wait(2000, stream) == pds.PDS_ETIMEOUT
+    assert pds.pds_component_sync(stream) == pds.PDS_OK
+    pds.pds_selftest_stuck_wait(2000, stream)
+    assert pds.pds_component_sync(stream) == pds.PDS_ETIMEOUT
     assert "gave up" in pds.last_error()
-    # the context is intact: a GEMM right after still runs and is right
+    assert pds.pds_component_sync(stream) == pds.PDS_OK  # read and cleared
     a = torch.randn(130, 128, device="cuda").to(torch.bfloat16)
     w = torch.randn(256, 128, device="cuda").to(torch.bfloat16)
     c = torch.empty(130, 256, device="cuda")
@@ -63,6 +67,6 @@ def test_stuck_device_wait_times_out_and_gpu_stays_usable():
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     pds.pds_gemm_bf16(a.data_ptr(), w.data_ptr(), c.data_ptr(), 130, 256, 128, ws.data_ptr(), wsb,
                       stream)
-    torch.cuda.synchronize()
+    assert pds.pds_component_sync(stream) == pds.PDS_OK
     ref = a.float() @ w.float().T
     assert float((c - ref).norm() / ref.norm()) < 1e-5

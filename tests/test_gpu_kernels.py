@@ -30,9 +30,10 @@ def test_gemm_bf16_matches_fp64(M, N, K):
     ws_bytes = pds.pds_gemm_workspace_bytes(M, N)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     for _ in range(2):  # second call reuses the scratch (counters must be back at zero)
+        stream = torch.cuda.current_stream().cuda_stream
         pds.pds_gemm_bf16(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K, ws.data_ptr(),
-                          ws_bytes, torch.cuda.current_stream().cuda_stream)
-        torch.cuda.synchronize()
+                          ws_bytes, stream)
+        assert pds.pds_component_sync(stream) == pds.PDS_OK
         want = a64 @ w64.T
         assert_parity(c.cpu().numpy(), want, f"gemm {M}x{N}x{K}", rel_l2=1e-5, max_abs_rms=1e-4)
 
@@ -50,8 +51,9 @@ def test_attention_matches_oracle(B, s, H, Hkv, hd):
     k, k64 = _bf16(rng, s + B, Hkv, hd)
     v, v64 = _bf16(rng, s + B, Hkv, hd)
     o = torch.full((B, H * hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
     pds.pds_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, s, H, Hkv, hd,
-                      torch.cuda.current_stream().cuda_stream)
-    torch.cuda.synchronize()
+                      stream)
+    assert pds.pds_component_sync(stream) == pds.PDS_OK
     want = oracle.causal_gqa_attention(q64, k64, v64, s).reshape(B, H * hd)
     assert_parity(bf16_to_f64(o), want, f"attention B={B} s={s} H={H}/{Hkv} hd={hd}")

@@ -42,7 +42,8 @@ def test_noalloc_gemm_matches_gemm_bf16_twice(M, N, K):
     for call in range(2):  # the second call finds the first call's leftovers in the scratch
         c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
         pds.pds_gemm_bf16_noalloc(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K, stream)
-        torch.cuda.synchronize()
+        # no bounded wait of the call gave up (the status word in the static scratch)
+        assert pds.pds_component_sync(stream) == pds.PDS_OK
         assert_parity(c.cpu().numpy(), want, f"noalloc call {call} {M}x{N}x{K}", rel_l2=1e-5,
                       max_abs_rms=1e-4)
 

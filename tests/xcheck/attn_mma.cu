@@ -1,3 +1,8 @@
+// TEST-ONLY cross-check (built into its own library, libpds_xcheck.so,
+// never into the product's libpds.so): a second, independent GPU
+// implementation of the stack's attention on the warp-level mma.sync tensor
+// path, for comparing the tcgen05 kernel against on the same inputs.
+//
 // GQA causal attention of the new rows over the cache prefix plus the new
 // rows (frink-models 0.29.0 src/decoder/cuda_prefill.rs, PrefillParams:
 // prefix_k / prefix_v are the cache's first start_pos rows; attn_scale =
@@ -15,9 +20,10 @@
 // h / (H / Hkv).
 #include <cuda_runtime.h>
 
+#include <math.h>
+#include <stdint.h>
+
 #include "common.cuh"
-#include "kernels.h"
-#include "tc.h"
 
 namespace pds {
 namespace {
@@ -298,16 +304,17 @@ cudaError_t launch_flash(const uint16_t* q, const uint16_t* k, const uint16_t* v
 
 }  // namespace
 
-pds_status tc_attention_mma(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                            uint16_t* o, int B, int start_pos, int H, int Hkv, int hd,
-                            cudaStream_t st, std::string* err) {
-  cudaError_t ce = hd == 128 ? launch_flash<128>(q, k, v, o, B, start_pos, H, Hkv, c.pdl, st)
-                             : launch_flash<64>(q, k, v, o, B, start_pos, H, Hkv, c.pdl, st);
-  if (ce != cudaSuccess) {
-    *err = std::string("attention launch: ") + cudaGetErrorString(ce);
-    return PDS_ELAUNCH;
-  }
-  return PDS_OK;
-}
-
 }  // namespace pds
+
+// 0 on success, else the cudaError_t of the failed launch.
+extern "C" int pdsx_attention_mma(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  uint16_t* o, int32_t batch, int32_t start_pos, int32_t n_heads,
+                                  int32_t n_kv_heads, int32_t head_dim, void* stream) {
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = head_dim == 128
+                       ? pds::launch_flash<128>(q, k, v, o, batch, start_pos, n_heads, n_kv_heads,
+                                                false, st)
+                       : pds::launch_flash<64>(q, k, v, o, batch, start_pos, n_heads, n_kv_heads,
+                                               false, st);
+  return static_cast<int>(ce);
+}
