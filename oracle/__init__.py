@@ -14,6 +14,7 @@ from .stack import (  # noqa: F401
     rms_norm,
     rope_inv_freq,
     rope_neox,
+    rope_rotate,
     silu,
     causal_gqa_attention,
     decoder_layer,

@@ -363,3 +363,226 @@ def test_inputs_are_seeded_and_row_stable():
         assert np.array_equal(l1[n], l1b[n])
     w = oracle.widen_bf16(l1["w_down"])
     assert abs(w.std() * math.sqrt(dims.ffn_dim) - 1.0) < 0.02
+
+
+# ------------------------------------------- attention extras and variants
+#
+# The optional parts of the launch descriptor (cuda_prefill.rs,
+# AttnExtrasCuda, LayerRopeCuda, PrefillParams.attn_softcap / window),
+# pinned by a second scalar restatement and by closed forms.
+
+def _bf_rope_general(head, pos, theta, layout, rot, ff, mscale):
+    # the first `rot` channels form rot/2 complex numbers, each turned by
+    # pos * theta**(-2i/rot) / ff[i] and scaled by mscale; the rest stay
+    out = list(head)
+    half = rot // 2
+    for i in range(half):
+        a, b = (i, i + half) if layout == "neox" else (2 * i, 2 * i + 1)
+        omega = theta ** (-2.0 * i / rot) / (ff[i] if ff is not None else 1.0)
+        z = complex(head[a], head[b]) * mscale * cmath.exp(1j * pos * omega)
+        out[a], out[b] = z.real, z.imag
+    return out
+
+
+def _bf_layer_variants(xs, w, kp, vp, s, H, Hkv, hd, theta, eps, layout, rot, ff, mscale,
+                       softcap, window):
+    W = {k: np.asarray(v).tolist() for k, v in w.items()}
+    keys = [[list(kp[j][g]) for g in range(Hkv)] for j in range(s)]
+    vals = [[list(vp[j][g]) for g in range(Hkv)] for j in range(s)]
+    qs, outs, krows, vrows = [], [], [], []
+
+    def heads(vec, nh, bias, gain, pos, rotate):
+        if bias is not None:
+            vec = [vec[i] + bias[i] for i in range(len(vec))]
+        hs = [vec[h * hd:(h + 1) * hd] for h in range(nh)]
+        if gain is not None:
+            hs = [_bf_rms(t, gain, eps) for t in hs]
+        if rotate:
+            hs = [_bf_rope_general(t, pos, theta, layout, rot, ff, mscale) for t in hs]
+        return hs
+
+    for b, x in enumerate(xs):
+        n = _bf_rms(x, W["attn_norm"], eps)
+        qh = heads(_bf_matvec(W["wq"], n), H, W.get("q_bias"), W.get("q_norm"), s + b, True)
+        kh = heads(_bf_matvec(W["wk"], n), Hkv, W.get("k_bias"), W.get("k_norm"), s + b, True)
+        vh = heads(_bf_matvec(W["wv"], n), Hkv, W.get("v_bias"), None, s + b, False)
+        qs.append(qh)
+        keys.append(kh)
+        vals.append(vh)
+        krows.append(kh)
+        vrows.append(vh)
+    for b, x in enumerate(xs):
+        p = s + b
+        o = []
+        for h in range(H):
+            g = h * Hkv // H
+            seen = [j for j in range(p + 1) if window is None or p - j < window]
+            sc = []
+            for j in seen:
+                z = sum(qs[b][h][c] * keys[j][g][c] for c in range(hd)) / math.sqrt(hd)
+                sc.append(softcap * math.tanh(z / softcap) if softcap is not None else z)
+            mx = max(sc)
+            e = [math.exp(t - mx) for t in sc]
+            tot = sum(e)
+            o.extend(sum(e[i] / tot * vals[seen[i]][g][c] for i in range(len(seen)))
+                     for c in range(hd))
+        att = _bf_matvec(W["wo"], o)
+        hrow = [x[i] + att[i] for i in range(len(x))]
+        m = _bf_rms(hrow, W["ffn_norm"], eps)
+        gt = _bf_matvec(W["w_gate"], m)
+        up = _bf_matvec(W["w_up"], m)
+        act = [gt[f] / (1.0 + math.exp(-gt[f])) * up[f] for f in range(len(gt))]
+        dn = _bf_matvec(W["w_down"], act)
+        outs.append([hrow[i] + dn[i] for i in range(len(x))])
+    return outs, krows, vrows
+
+
+VARIANTS = {
+    "extras": dict(extras=True),
+    "norm-layout": dict(rope_layout="norm"),
+    "partial-rot-factors-mscale": dict(rot_dim=4, freq_factors=[1.0, 8.0], rope_mscale=1.3),
+    "norm-partial": dict(rope_layout="norm", rot_dim=4, extras=True),
+    "softcap-window": dict(attn_softcap=0.9, window=3),
+    "everything": dict(extras=True, rope_layout="norm", rot_dim=4, freq_factors=[2.0, 0.5],
+                       rope_mscale=0.8, attn_softcap=1.5, window=4),
+}
+
+
+@pytest.mark.parametrize("s", [0, 3])
+@pytest.mark.parametrize("name", sorted(VARIANTS))
+def test_stack_variants_match_brute_force(name, s):
+    opts = dict(VARIANTS[name])
+    extras = opts.pop("extras", False)
+    rng = np.random.default_rng(23)
+    d, H, Hkv, hd, F, B, L = 8, 4, 2, 8, 12, 3, 2
+    theta, eps = 37.0, 1e-5
+    layers = [_micro_layer(rng, d, H, Hkv, hd, F) for _ in range(L)]
+    if extras:
+        for w in layers:
+            w["q_bias"] = 0.3 * _rand(rng, H * hd)
+            w["k_bias"] = 0.3 * _rand(rng, Hkv * hd)
+            w["v_bias"] = 0.3 * _rand(rng, Hkv * hd)
+            w["q_norm"] = 1.0 + 0.2 * _rand(rng, hd)
+            w["k_norm"] = 1.0 + 0.2 * _rand(rng, hd)
+    pk = [_rand(rng, s, Hkv, hd) for _ in range(L)]
+    pv = [_rand(rng, s, Hkv, hd) for _ in range(L)]
+    x0 = _rand(rng, B, d)
+    got, gk, gv = oracle.prefill_dense_stack(x0, layers, pk, pv, s, H, Hkv, hd, theta, eps,
+                                             **opts)
+    bf = dict(layout=opts.get("rope_layout", "neox"), rot=opts.get("rot_dim") or hd,
+              ff=opts.get("freq_factors"), mscale=opts.get("rope_mscale", 1.0),
+              softcap=opts.get("attn_softcap"), window=opts.get("window"))
+    xs = x0.tolist()
+    for l in range(L):
+        xs, kr, vr = _bf_layer_variants(xs, layers[l], pk[l].tolist(), pv[l].tolist(), s, H,
+                                        Hkv, hd, theta, eps, **bf)
+        np.testing.assert_allclose(gk[l], np.array(kr), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(gv[l], np.array(vr), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got, np.array(xs), rtol=0, atol=1e-11)
+
+
+def test_norm_layout_is_neox_on_interleaved_channels():
+    # moving channel 2i to i and 2i+1 to i + hd/2 turns the Norm layout into Neox
+    rng = np.random.default_rng(5)
+    hd = 8
+    t = _rand(rng, 4, 3, hd)
+    pos = np.array([0, 1, 7, 40])
+    perm = np.concatenate([np.arange(0, hd, 2), np.arange(1, hd, 2)])
+    got = oracle.rope_rotate(t, pos, 1e4, layout="norm")
+    want = oracle.rope_rotate(t[..., perm], pos, 1e4, layout="neox")
+    np.testing.assert_allclose(got[..., perm], want, rtol=0, atol=1e-13)
+    with pytest.raises(ValueError):
+        oracle.rope_rotate(t, pos, 1e4, layout="bogus")
+
+
+@pytest.mark.parametrize("layout", ["neox", "norm"])
+def test_partial_rotation_leaves_the_tail_and_rotates_the_head_as_a_smaller_rope(layout):
+    rng = np.random.default_rng(6)
+    hd, rot = 16, 8
+    t = _rand(rng, 5, 2, hd)
+    pos = np.arange(5) * 3 + 1
+    got = oracle.rope_rotate(t, pos, 500.0, layout=layout, rot_dim=rot)
+    np.testing.assert_array_equal(got[..., rot:], t[..., rot:])
+    np.testing.assert_allclose(got[..., :rot], oracle.rope_rotate(t[..., :rot], pos, 500.0,
+                                                                  layout=layout),
+                               rtol=0, atol=1e-13)
+
+
+def test_freq_factors_divide_the_angle_and_mscale_scales_the_rotated_channels():
+    rng = np.random.default_rng(7)
+    hd = 8
+    t = _rand(rng, 3, 2, hd)
+    pos = np.array([2.0, 6.0, 10.0])
+    c = 4.0
+    # a common factor c is the same as positions p / c
+    np.testing.assert_allclose(oracle.rope_rotate(t, pos, 1e4, freq_factors=[c] * (hd // 2)),
+                               oracle.rope_rotate(t, pos / c, 1e4), rtol=0, atol=1e-13)
+    # the angular frequencies themselves
+    np.testing.assert_allclose(oracle.rope_inv_freq(8, 100.0, [1, 2, 4, 8]),
+                               [1.0, 100 ** -0.25 / 2, 100 ** -0.5 / 4, 100 ** -0.75 / 8])
+    # mscale multiplies the norm of every rotated pair
+    got = oracle.rope_rotate(t, pos, 1e4, rot_dim=4, mscale=1.7)
+    for i in range(2):
+        a = np.hypot(got[..., i], got[..., i + 2])
+        np.testing.assert_allclose(a, 1.7 * np.hypot(t[..., i], t[..., i + 2]), rtol=1e-13)
+    np.testing.assert_array_equal(got[..., 4:], t[..., 4:])
+
+
+def test_window_of_one_row_returns_the_rows_own_value():
+    rng = np.random.default_rng(8)
+    B, s, H, Hkv, hd = 4, 5, 4, 2, 8
+    q = _rand(rng, B, H, hd)
+    k = _rand(rng, s + B, Hkv, hd)
+    v = _rand(rng, s + B, Hkv, hd)
+    o = oracle.causal_gqa_attention(q, k, v, s, window=1)
+    for b in range(B):
+        for h in range(H):
+            np.testing.assert_allclose(o[b, h], v[s + b, h // 2], rtol=0, atol=1e-14)
+    # a window at least as long as every row's history changes nothing
+    np.testing.assert_allclose(oracle.causal_gqa_attention(q, k, v, s, window=s + B),
+                               oracle.causal_gqa_attention(q, k, v, s), rtol=0, atol=0)
+
+
+def test_softcap_bounds_the_scores_and_vanishes_for_a_wide_cap():
+    rng = np.random.default_rng(9)
+    B, s, H, Hkv, hd = 3, 2, 2, 1, 4
+    q = 4.0 * _rand(rng, B, H, hd)
+    k = 4.0 * _rand(rng, s + B, Hkv, hd)
+    v = _rand(rng, s + B, Hkv, hd)
+    base = oracle.causal_gqa_attention(q, k, v, s)
+    wide = oracle.causal_gqa_attention(q, k, v, s, softcap=1e6)
+    np.testing.assert_allclose(wide, base, rtol=0, atol=1e-9)
+    # with a cap far below the scores every visible key scores about +-cap:
+    # two keys, row 0 at s=0 sees key 0 only, row 1 sees two nearly equal weights
+    # when both raw scores are large and positive
+    q2 = np.ones((2, 1, 4)) * 10.0
+    k2 = np.ones((2, 1, 4)) * np.array([[[3.0]], [[5.0]]])
+    v2 = np.array([[[1.0, 0, 0, 0]], [[0, 1.0, 0, 0]]])
+    o2 = oracle.causal_gqa_attention(q2, k2, v2, 0, softcap=1e-3)
+    np.testing.assert_allclose(o2[1, 0, :2], [0.5, 0.5], atol=1e-6)
+
+
+def test_biases_and_qk_norm_closed_forms():
+    rng = np.random.default_rng(10)
+    d, H, Hkv, hd, F, B = 8, 2, 1, 8, 12, 3
+    w = _micro_layer(rng, d, H, Hkv, hd, F)
+    # zero projections: the K/V rows are the rotated k bias and the v bias
+    for n in ("wq", "wk", "wv"):
+        w[n] = np.zeros_like(w[n])
+    w["q_bias"] = _rand(rng, H * hd)
+    w["k_bias"] = _rand(rng, Hkv * hd)
+    w["v_bias"] = _rand(rng, Hkv * hd)
+    x = _rand(rng, B, d)
+    empty = np.zeros((0, Hkv, hd))
+    _, k, v = oracle.decoder_layer(x, w, empty, empty, 0, H, Hkv, hd, 1e4, 1e-5)
+    pos = np.arange(B)
+    np.testing.assert_allclose(v, np.broadcast_to(w["v_bias"].reshape(1, Hkv, hd), v.shape),
+                               rtol=0, atol=0)
+    want_k = oracle.rope_rotate(np.broadcast_to(w["k_bias"].reshape(1, Hkv, hd), k.shape), pos,
+                                1e4)
+    np.testing.assert_allclose(k, want_k, rtol=0, atol=1e-14)
+    # unit k_norm gain: every rotated k head has RMS 1 (eps aside; RoPE keeps norms)
+    w2 = _micro_layer(rng, d, H, Hkv, hd, F)
+    w2["k_norm"] = np.ones(hd)
+    _, k2, _ = oracle.decoder_layer(x, w2, empty, empty, 0, H, Hkv, hd, 1e4, 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(k2 ** 2, axis=-1)), 1.0, rtol=1e-12)
