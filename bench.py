@@ -14,10 +14,13 @@ d=3072, 24/8 heads of 128, ffn 8192, 512 new tokens, empty prefix).
   after W warm-up steps; weights (5.6 GB) exceed the 129 MB L2, so no flush.
 * ``e2e``: the same through the host-I/O entry point (pinned host hidden
   batch in, host out; the copies are inside the timed region).
-* ``roofline``: the dominant kernel, its algorithmic FLOP per launch over
-  its average CUDA-event duration (measured in a pass right after the timed
-  region, with per-kernel events on the call's stream), against the measured
-  sustained bf16 peak.
+* ``roofline``: the dominant kernel, its algorithmic FLOP (or bytes) per
+  launch over its average CUDA-event duration (measured in a pass right
+  after the timed region, with per-kernel events on the call's stream),
+  against the measured bf16 peak (burst for a timed region shorter than a
+  second, else sustained) or, for a workload whose GEMMs stream weights
+  (batch below the ridge of the two peaks), the measured HBM bandwidth.
+  ``kernels`` gives every kernel kind's achieved TFLOP/s and GB/s.
 * ``cpu_baseline``: the fp64 CPU oracle on a bounded sample (the first
   layers of the same workload), extrapolated to the whole stack.
 
@@ -63,7 +66,34 @@ def flops(dims):
     return per, dims.n_layers * sum(per.values())
 
 
-KERNEL_SOURCES = ("gemm_tc.cu", "sm100.cuh", "attn_tc.cu", "attn.cu", "tc.h", "kernels.h",
+def weight_bytes_per_layer(dims):
+    d, F, qw, kvw = dims.d_model, dims.ffn_dim, dims.q_width, dims.kv_width
+    return 2 * (d * (qw + 2 * kvw) + qw * d + 2 * F * d + F * d) + 4 * 2 * d
+
+
+def algo_bytes(dims):
+    """Bytes each kernel kind must move at least once per launch: weights and
+    cache rows read, activations read and written (float32 4, bf16 2), once."""
+    B, s, d, F, hd = dims.batch, dims.start_pos, dims.d_model, dims.ffn_dim, dims.head_dim
+    qw, kvw = dims.q_width, dims.kv_width
+    ss = 4 * B * (d // 64)  # row sum-of-squares partials
+    return {
+        # weights, a, ss in; q and the new k/v rows out
+        "qkv": 2 * d * (qw + 2 * kvw) + 2 * B * d + ss + 2 * B * qw + 2 * 2 * B * kvw,
+        # q in, every visible K/V row once, o out
+        "attn": 2 * B * qw + 2 * 2 * (s + B) * kvw + 2 * B * qw,
+        # weights, o in; residual in, h and a = bf16(h*g) and ss out
+        "wo": 2 * qw * d + 2 * B * qw + 4 * B * d + 4 * B * d + 2 * B * d + ss,
+        # weights, a and ss in; act out
+        "gateup": 2 * 2 * F * d + 2 * B * d + ss + 2 * B * F,
+        # weights, act in; residual in, x' and a and ss out
+        "down": 2 * F * d + 2 * B * F + 4 * B * d + 4 * B * d + 2 * B * d + ss,
+        # prep: x and the gain in, a and ss out; the (cos, sin) table out
+        "prep": 4 * B * d + 4 * d + 2 * B * d + ss + 8 * B * (hd // 2),
+    }
+
+
+KERNEL_SOURCES = ("gemm_tc.cu", "sm100.cuh", "attn_tc.cu", "prep.cu", "tc.h", "kernels.h",
                   "common.cuh")
 
 
@@ -325,16 +355,27 @@ def main():
     kt = pds.pds_plan_kernel_times(st.plan, stream.cuda_stream, reset=True)
     pds.pds_plan_set_timing(st.plan, False)
     per_flop, total_flop = flops(dims)
+    per_bytes = algo_bytes(dims)
     peaks, peak_src = read_peaks()
-    peak_tf = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # A kernel timed inside a timed region shorter than a second runs at the
+    # burst clocks: its denominator is the burst peak (the sustained one is
+    # printed beside it).
+    timed_s = ms_per_step * args.steps / 1e3
+    burst = timed_s < 1.0
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sust = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_tf = peak_burst if burst else peak_sust
+    peak_gbs = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     kernels = {}
     for kind, (n, tot) in kt.items():
         if n == 0:
             continue
         avg_ms = tot / n
-        k = {"launches": n, "avg_us": avg_ms * 1e3, "share": None}
+        k = {"launches": n, "avg_us": avg_ms * 1e3, "share": None,
+             "gbs": per_bytes[kind] / (avg_ms / 1e3) / 1e9}
         if kind in per_flop:
             k["tflops"] = per_flop[kind] / (avg_ms / 1e3) / 1e12
+        k["hbm_frac"] = k["gbs"] / peak_gbs
         kernels[kind] = k
     tot_all = sum(v[1] for v in kt.values()) or 1.0
     for kind, k in kernels.items():
@@ -343,19 +384,42 @@ def main():
     dom = max(gemm_kinds, key=lambda k: kt[k][1])
     gemm_ms = sum(kt[k][1] for k in gemm_kinds) / args.steps
     gemm_flop = dims.n_layers * sum(per_flop[k] for k in gemm_kinds)
-    roofline = {
-        "kernel": f"gemm_{dom}", "bound": "tensor",
-        "achieved": kernels[dom]["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
-        "frac": kernels[dom]["tflops"] / peak_tf,
+    # a GEMM of M rows does M flop per weight byte: below the ridge of the
+    # measured peaks (flop per byte at which both peaks meet) it streams
+    # weights and is bound by HBM, above it by the tensor cores
+    ridge = peak_tf * 1e12 / (peak_gbs * 1e9)
+    hbm_bound = dims.batch < ridge
+    if hbm_bound:
+        roofline = {
+            "kernel": f"gemm_{dom}", "bound": "hbm",
+            "achieved": kernels[dom]["gbs"], "peak": peak_gbs, "unit": "GB/s",
+            "frac": kernels[dom]["gbs"] / peak_gbs,
+            "peak_source": f"{peak_src} hbm_gbs",
+        }
+    else:
+        roofline = {
+            "kernel": f"gemm_{dom}", "bound": "tensor",
+            "achieved": kernels[dom]["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
+            "frac": kernels[dom]["tflops"] / peak_tf,
+            "peak_source": f"{peak_src} {'bf16_tflops (burst)' if burst else 'bf16_tflops_sustained'}"
+                           f": timed region {timed_s:.2f} s",
+            "frac_of_sustained": kernels[dom]["tflops"] / peak_sust,
+        }
+    roofline.update({
         "traffic": measured_traffic(dom, args.workload), "traffic_unit": "bytes per launch",
-        "peak_source": f"{peak_src} bf16_tflops_sustained",
+        "algorithmic_bytes": per_bytes[dom], "algorithmic_flop": per_flop[dom],
         "gemm_frac": gemm_flop / (gemm_ms / 1e3) / 1e12 / peak_tf,
         # the GEMMs' share of the replayed step: the step less the other
         # kernels' stand-alone times (launch gaps and overlaps go to the GEMMs)
         "gemm_frac_in_step": gemm_flop / ((ms_per_step - sum(
             kt[k][1] for k in kt if k not in gemm_kinds) / args.steps) / 1e3) / 1e12 / peak_tf,
         "end_to_end_frac": total_flop / (ms_per_step / 1e3) / 1e12 / peak_tf,
-    }
+        # every byte a step must move at least once (weights, caches read,
+        # activations in and out) over the step's time, against HBM
+        "step_hbm_frac": dims.n_layers * sum(per_bytes[k] for k in per_flop) /
+                         (ms_per_step / 1e3) / 1e9 / peak_gbs,
+    })
+    weight_bytes = dims.n_layers * weight_bytes_per_layer(dims)
 
     if rank != 0:
         return
@@ -365,9 +429,13 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1/in) bf16 weights, N(0,1) hidden)",
         "config": {"workload": args.workload, **_cfg(dims),
-                   "l2": "inputs larger than L2: 5.6 GB of weights stream every step, no flush",
+                   "l2": (f"inputs larger than L2: {weight_bytes / 1e9:.2f} GB of weights "
+                          f"stream every step against a 129 MB L2, no flush"
+                          if weight_bytes > 2 * 129e6 else
+                          f"{weight_bytes / 1e6:.1f} MB of weights: L2-resident between steps"),
                    "parallelism": f"replicas x{world}"},
         "tflops": total_flop / (ms_per_step / 1e3) / 1e12,
+        "us_per_token": ms_per_step * 1e3 / B,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": B * dims.d_model * 4,
                 "d2h_bytes_per_step": B * dims.d_model * 4},
         "gpu_launches": args.steps * (2 + 5 * dims.n_layers),

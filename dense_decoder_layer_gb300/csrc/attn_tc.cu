@@ -1,9 +1,12 @@
 // GQA causal attention of the new rows over the cache prefix plus the new
 // rows, on the tcgen05 tensor cores (frink-models 0.29.0
 // src/decoder/cuda_prefill.rs, PrefillParams: prefix_k / prefix_v are the
-// cache's first start_pos rows; attn_scale = 1/sqrt(head_dim); no softcap,
-// no window).  Query row b sits at position start_pos + b and reads kv head
-// h / (H / Hkv).
+// cache's first start_pos rows; attn_scale = 1/sqrt(head_dim); attn_softcap;
+// window).  Query row b sits at position p = start_pos + b, reads kv head
+// h / (H / Hkv) and sees keys j <= p (with a window, p - window < j <= p
+// only: key tiles wholly below a query tile's windows are not visited).  A
+// softcap turns a scaled score z into cap * tanh(z / cap) before the
+// softmax.
 //
 // One CTA per (query head, 128 query rows), heaviest row tiles first.
 //   warp 0      TMA producer: the Q tile once, then K and V tiles of 128
@@ -79,13 +82,77 @@ struct AttnCfg {
 struct AttnMaps {
   CUtensorMap q, k, v;
 };
+
+// 2^x on the special-function unit (approximate, subnormal results flushed).
+__device__ __forceinline__ float exp2_sfu_raw(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 struct AttnArgs {
   uint16_t* o;
   int B, s, H, Hkv;
   float scale_log2;
   uint32_t* status;
   int n_split;  // the first (heaviest) n_split tiles are split over a CTA pair
+  float cap_raw;  // softcap over the score scale (raw q.k units); 0: none
+  int window;     // 0: none
+  // Chunked key ranges (long prefixes): every query tile's key range is cut
+  // into ceil(span / chunk) equal chunks, one CTA each, which writes its
+  // unnormalised O and its rows' (reference maximum, sum) to o_part /
+  // ml_part at its unit; attn_merge_kernel combines them.  0: off.
+  int chunk;
+  float* o_part;    // [units][128 rows][HD] float32
+  float2* ml_part;  // [units][128 rows]
 };
+
+// First key tile a query tile starting at position p0 visits: the one that
+// holds its first row's first visible key.
+__host__ __device__ __forceinline__ int first_key_tile(int p0, int window) {
+  return window > 0 ? max(0, p0 - window + 1) / kKeys : 0;
+}
+
+// Key tiles [first, first + span) of query tile qt (rows qt*128 ..).
+__host__ __device__ __forceinline__ void key_span(int qt, int B, int s, int window, int& first,
+                                                  int& span) {
+  const int last_row = min((qt + 1) * kRows, B) - 1;
+  const int nkt = (s + last_row + 1 + kKeys - 1) / kKeys;
+  first = first_key_tile(s + qt * kRows, window);
+  span = nkt - first;
+}
+
+// Unit u of the chunked mode: query tiles from the last (longest) to the
+// first, and within one the chunks, heads fastest.  Sets the query tile,
+// head, chunk, chunk count and the chunk's key tiles [kt0, kt0 + n).
+__host__ __device__ __forceinline__ bool chunk_unit(int u, int B, int s, int H, int window,
+                                                    int chunk, int& qt, int& h, int& c, int& nc,
+                                                    int& kt0, int& n) {
+  const int nq = (B + kRows - 1) / kRows;
+  int base = 0;
+  for (qt = nq - 1; qt >= 0; --qt) {
+    int first, span;
+    key_span(qt, B, s, window, first, span);
+    nc = (span + chunk - 1) / chunk;
+    if (u < base + nc * H) {
+      const int local = u - base;
+      c = local / H;
+      h = local - c * H;
+      kt0 = first + (c * span) / nc;
+      n = first + ((c + 1) * span) / nc - kt0;
+      return true;
+    }
+    base += nc * H;
+  }
+  return false;
+}
+
+// c * tanh(x / c) from the identity tanh(y) = 1 - 2 / (e^(2y) + 1), with
+// e^(2y) = 2^(x * k2) on the special-function unit (k2 = 2 log2(e) / c);
+// it tends to +-c as |x| grows.
+__device__ __forceinline__ float softcap_raw(float x, float c, float k2) {
+  const float e = exp2_sfu_raw(x * k2);
+  return c - __fdividef(2.0f * c, e + 1.0f);
+}
 
 // K-major SW128 descriptor of a 128-row operand whose K extent is split in
 // 64-element (128-byte) column blocks of 16 KB each.
@@ -110,12 +177,7 @@ __device__ __forceinline__ uint64_t v_desc(uint32_t base, int kstep) {
   return d;
 }
 
-// 2^x on the special-function unit (approximate, subnormal results flushed).
-__device__ __forceinline__ float exp2_sfu(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+__device__ __forceinline__ float exp2_sfu(float x) { return exp2_sfu_raw(x); }
 
 // Pairwise (tree) maximum and sum of n values.
 template <int N>
@@ -141,7 +203,9 @@ __host__ __device__ constexpr uint32_t idesc_attn(int M, int N, bool b_mn) {
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-template <int HD>
+// VAR: the run has a softcap or a window (the plain instantiation carries
+// no code for either).
+template <int HD, bool VAR>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_tc_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ AttnArgs a) {
   using namespace sm100;
@@ -184,14 +248,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (t >= a.H * nq) return;
     }
   }
-  const int qt = nq - 1 - t / a.H;
-  const int h = t % a.H, g = h / (a.H / a.Hkv);
+  int qt = nq - 1 - t / a.H;
+  int h = t % a.H;
+  int kt0, n;  // this CTA's key tiles [kt0, kt0 + n)
+  const bool chunked = a.chunk > 0;
+  if (chunked) {
+    int c, nc;
+    if (!chunk_unit(blockIdx.y, a.B, a.s, a.H, VAR ? a.window : 0, a.chunk, qt, h, c, nc, kt0, n))
+      return;
+  } else {
+    const int last_row = min(qt * kRows + kRows, a.B) - 1;
+    const int nkt = (a.s + last_row + 1 + kKeys - 1) / kKeys;  // key tiles up to the last row's
+    const int kf = VAR ? first_key_tile(a.s + qt * kRows, a.window) : 0;  // first visited
+    const int span = nkt - kf;
+    const int nk0 = (span + 1) / 2;
+    kt0 = kf + ((split && half == 1) ? nk0 : 0);
+    n = split ? (half == 0 ? nk0 : span - nk0) : span;
+  }
+  const int g = h / (a.H / a.Hkv);
   const int b0 = qt * kRows;
-  const int last_row = min(b0 + kRows, a.B) - 1;
-  const int nkt = (a.s + last_row + 1 + kKeys - 1) / kKeys;  // key tiles of the query tile
-  const int nk0 = (nkt + 1) / 2;
-  const int kt0 = (split && half == 1) ? nk0 : 0;                   // first key tile of this CTA
-  const int n = split ? (half == 0 ? nk0 : nkt - nk0) : nkt;        // its key tiles
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -333,12 +408,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_s_free(st));
-        // causal mask and this part's maximum
+        if (VAR && a.cap_raw > 0.f) {
+          const float k2 = 2.0f * 1.4426950408889634f / a.cap_raw;
+#pragma unroll
+          for (int i = 0; i < kPartKeys; ++i) sv[i] = softcap_raw(sv[i], a.cap_raw, k2);
+        }
+        // causal mask (and window) and this part's maximum
         const int rel = rel0 - j * kKeys;  // key i of the part is past the row: i > rel
         if (kPartKeys - 1 > rel - r) {      // some key past some row of the tile
 #pragma unroll
           for (int i = 0; i < kPartKeys; ++i)
             if (i > rel) sv[i] = -INFINITY;
+        }
+        if (VAR && a.window > 0) {  // key i is at or below the window's start: i <= rel - window
+          const int lo = rel - a.window;
+#pragma unroll
+          for (int i = 0; i < kPartKeys; ++i)
+            if (i <= lo) sv[i] = -INFINITY;
         }
         mx = tree_max<kPartKeys>(sv);
       }
@@ -420,7 +506,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       return o_row + (static_cast<uint32_t>(c ^ (r & (kPartChunks - 1))) << 4);
     };
     float* lmsg = reinterpret_cast<float*>(smem + C::kP0);  // [128] row sums, then [128] maxima
-    if (split && half == 1) {
+    if (chunked) {
+      // this chunk's unnormalised O row part and the row's (reference max, sum)
+      if (ok) {
+        float* dst = a.o_part + (static_cast<size_t>(blockIdx.y) * kRows + r) * HD + part * kPartCols;
+#pragma unroll
+        for (int c = 0; c < kPartCols / 16; ++c) {
+          float t[16];
+          tmem_load16(tmem + lane_off + 256u + part * kPartCols + c * 16, t);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            __stcg(reinterpret_cast<float4*>(dst + c * 16) + i,
+                   make_float4(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]));
+        }
+        if (part == 0) __stcg(a.ml_part + static_cast<size_t>(blockIdx.y) * kRows + r,
+                              make_float2(m_ref, l));
+      }
+    } else if (split && half == 1) {
       if (ok) {
 #pragma unroll
         for (int c = 0; c < kPartCols / 16; ++c) {
@@ -457,9 +559,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       wait(bar_m_recv, 0);
       if (ok) {
+        // a row sees its own key, in one half or the other: m is finite (a
+        // half that sees none of the row's keys has maximum -inf, weight 0)
         const float m1 = lmsg[128 + r];
-        const float m = fmaxf(m_ref, m1);  // m_ref: key 0 is in the first half, finite
-        const float a0 = exp2f(m_ref - m);
+        const float m = fmaxf(m_ref, m1);
+        const float a0 = m_ref == -INFINITY ? 0.f : exp2f(m_ref - m);
         const float a1 = m1 == -INFINITY ? 0.f : exp2f(m1 - m);
         const float inv = 1.f / (l * a0 + lmsg[r] * a1);
         const int b = b0 + r;
@@ -522,12 +626,103 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// Combines the chunks of the chunked mode: for each query tile, row and
+// head, O = sum_c O_c 2^(m_c - m) / sum_c l_c 2^(m_c - m), m = max_c m_c, in
+// chunk order.  One warp per (query tile, head, row); lane i holds columns
+// 4i .. 4i + 3.
 template <int HD>
+__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnArgs a) {
+  sm100::grid_dep_wait();
+  sm100::grid_dep_launch();
+  const int warp = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int nq = (a.B + kRows - 1) / kRows;
+  const int r = warp % kRows;
+  int rest = warp / kRows;
+  const int h = rest % a.H;
+  const int tq = rest / a.H;  // 0: the last query tile (units are ordered that way)
+  if (tq >= nq) return;
+  const int qt = nq - 1 - tq;
+  const int b = qt * kRows + r;
+  if (b >= a.B || 4 * lane >= HD) return;
+  // the units of this query tile: those of the later (longer) tiles come first
+  int base = 0, first = 0, span = 0, nc = 0;
+  for (int q = nq - 1; q >= qt; --q) {
+    key_span(q, a.B, a.s, a.window, first, span);
+    nc = (span + a.chunk - 1) / a.chunk;
+    if (q > qt) base += nc * a.H;
+  }
+  float m = -INFINITY;
+  for (int c = 0; c < nc; ++c)
+    m = fmaxf(m, a.ml_part[static_cast<size_t>(base + c * a.H + h) * kRows + r].x);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  for (int c = 0; c < nc; ++c) {
+    const size_t u = static_cast<size_t>(base + c * a.H + h);
+    const float2 ml = a.ml_part[u * kRows + r];
+    if (ml.x == -INFINITY) continue;  // the row sees no key of this chunk
+    const float w = exp2f(ml.x - m);
+    const float4 o = __ldcg(reinterpret_cast<const float4*>(a.o_part + (u * kRows + r) * HD) + lane);
+    acc.x += o.x * w;
+    acc.y += o.y * w;
+    acc.z += o.z * w;
+    acc.w += o.w * w;
+    l += ml.y * w;
+  }
+  const float inv = 1.f / l;
+  uint16_t* dst = a.o + (static_cast<size_t>(b) * a.H + h) * HD + 4 * lane;
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+}
+
+// Per-CTA cost beyond its key tiles (prologue, Q load, the partial rows'
+// stores), in key-tile times, for the chunk chooser.
+constexpr int kChunkOverheadTiles = 3;
+// Chunks are at least this many key tiles.
+constexpr int kMinChunkTiles = 4;
+
+// Key tiles per chunk for the chunked mode, or 0 when it does not pay: the
+// time of a schedule is its waves of resident CTAs times the longest chunk
+// plus a CTA's overhead; the chunked mode must beat one CTA per query tile
+// by a fifth (the CTA-pair split covers the middle ground).
+int choose_chunk(int B, int s, int H, int window, int num_sms, int max_units) {
+  const int nq = (B + kRows - 1) / kRows;
+  int span_max = 0;
+  for (int qt = 0; qt < nq; ++qt) {
+    int first, span;
+    key_span(qt, B, s, window, first, span);
+    span_max = std::max(span_max, span);
+  }
+  if (num_sms < 1 || max_units < 1) return 0;
+  const double waves0 = std::ceil(static_cast<double>(H) * nq / num_sms);
+  double best = 0.8 * waves0 * (span_max + kChunkOverheadTiles);
+  int best_c = 0;
+  for (int c = span_max - 1; c >= kMinChunkTiles; --c) {
+    long long units = 0;
+    int longest = 0;
+    for (int qt = 0; qt < nq; ++qt) {
+      int first, span;
+      key_span(qt, B, s, window, first, span);
+      const int nc = (span + c - 1) / c;
+      units += static_cast<long long>(nc) * H;
+      longest = std::max(longest, (span + nc - 1) / nc);
+    }
+    if (units > max_units) break;  // smaller chunks only make more units
+    const double cost = std::ceil(static_cast<double>(units) / num_sms) *
+                        (longest + kChunkOverheadTiles);
+    if (cost < best) {
+      best = cost;
+      best_c = c;
+    }
+  }
+  return best_c;
+}
+
+template <int HD, bool VAR>
 pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                          uint16_t* o, int B, int s, int H, int Hkv, cudaStream_t st,
-                          std::string* err) {
+                          uint16_t* o, int B, int s, int H, int Hkv, float softcap, int window,
+                          cudaStream_t st, std::string* err) {
   using C = AttnCfg<HD>;
-  const void* fn = reinterpret_cast<const void*>(attn_tc_kernel<HD>);
+  const void* fn = reinterpret_cast<const void*>(attn_tc_kernel<HD, VAR>);
   const cudaError_t attr = kernel_smem_attr(fn, static_cast<int>(C::kSmem));
   if (attr != cudaSuccess) {
     *err = std::string("attention shared-memory attribute: ") + cudaGetErrorString(attr);
@@ -543,19 +738,61 @@ pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, co
   if ((rc = tc_map_bf16(c, &maps.v, v, static_cast<uint64_t>(Hkv) * HD, T, 128, err)) != PDS_OK)
     return rc;
   AttnArgs args{o, B, s, H, Hkv, 1.4426950408889634f / sqrtf(static_cast<float>(HD)), c.status,
-                0};
+                0, softcap > 0.f ? softcap * sqrtf(static_cast<float>(HD)) : 0.f, window,
+                0, nullptr, nullptr};
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
+  const int nq = (B + kRows - 1) / kRows, tiles = H * nq;
+  // Long key ranges: equal chunks over all SMs, merged by a second kernel.
+  const int max_units =
+      static_cast<int>(std::min<size_t>(c.attn_ws_bytes / tc_attention_unit_bytes(HD), 1 << 20));
+  const int chunk = choose_chunk(B, s, H, VAR ? window : 0, c.num_sms, max_units);
+  if (chunk > 0) {
+    int units = 0;
+    for (int qt = 0; qt < nq; ++qt) {
+      int first, span;
+      key_span(qt, B, s, VAR ? window : 0, first, span);
+      units += H * ((span + chunk - 1) / chunk);
+    }
+    args.chunk = chunk;
+    args.o_part = reinterpret_cast<float*>(c.attn_ws);
+    args.ml_part = reinterpret_cast<float2*>(c.attn_ws + static_cast<size_t>(units) * kRows * HD * 4);
+    cudaLaunchAttribute at[1];
+    int na = 0;
+    if (c.pdl) {
+      at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      at[na].val.programmaticStreamSerializationAllowed = 1;
+      ++na;
+    }
+    cfg.gridDim = dim3(1, units);
+    cfg.attrs = at;
+    cfg.numAttrs = na;
+    cudaError_t ce = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, VAR>, maps, args);
+    if (ce == cudaSuccess) {
+      cudaLaunchConfig_t mc = {};
+      mc.gridDim = dim3((tiles * kRows + 7) / 8);
+      mc.blockDim = dim3(256);
+      mc.stream = st;
+      mc.attrs = at;
+      mc.numAttrs = na;
+      ce = cudaLaunchKernelEx(&mc, attn_merge_kernel<HD>, args);
+    }
+    if (ce != cudaSuccess) {
+      *err = std::string("attention launch: ") + cudaGetErrorString(ce);
+      return PDS_ELAUNCH;
+    }
+    return PDS_OK;
+  }
   // Split the longest query tiles (a whole row of tiles over the heads at a
   // time) while every CTA still has an SM of its own: fewer tiles than SMs
   // otherwise leave SMs idle behind the longest tiles.
-  const int nq = (B + kRows - 1) / kRows, tiles = H * nq;
   const int pair_cap = std::min(c.num_sms / 2, kernel_max_clusters(fn, cfg, 2));
   int n_split = 0;
   for (int qt = nq - 1; qt >= 0; --qt) {
-    const int nkt = (s + std::min((qt + 1) * kRows, B) + kKeys - 1) / kKeys;
+    const int nkt = (s + std::min((qt + 1) * kRows, B) + kKeys - 1) / kKeys -
+                    first_key_tile(s + qt * kRows, window);
     const int n = n_split + H;
     if (nkt < kSplitMinKeyTiles || n + (tiles - n + 1) / 2 > pair_cap) break;
     n_split = n;
@@ -580,7 +817,7 @@ pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, co
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  cudaError_t ce = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD>, maps, args);
+  cudaError_t ce = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, VAR>, maps, args);
   if (ce != cudaSuccess) {
     *err = std::string("attention launch: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;
@@ -590,11 +827,32 @@ pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, co
 
 }  // namespace
 
+size_t tc_attention_unit_bytes(int hd) { return static_cast<size_t>(kRows) * (hd * 4 + 8); }
+
+size_t tc_attention_scratch_bytes(int B, int s, int H, int hd) {
+  // the most units the chunked mode can use: chunks of at least
+  // kMinChunkTiles key tiles, and no more than 8 per query tile and head
+  const int nq = (B + kRows - 1) / kRows;
+  long long units = 0;
+  for (int qt = 0; qt < nq; ++qt) {
+    int first, span;
+    key_span(qt, B, s, 0, first, span);
+    units += static_cast<long long>(H) * std::min(8, span / kMinChunkTiles);
+  }
+  return static_cast<size_t>(units) * tc_attention_unit_bytes(hd);
+}
+
 pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                        uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
-                        std::string* err) {
-  return hd == 128 ? launch_attn_tc<128>(c, q, k, v, o, B, start_pos, H, Hkv, st, err)
-                   : launch_attn_tc<64>(c, q, k, v, o, B, start_pos, H, Hkv, st, err);
+                        uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, float softcap,
+                        int window, cudaStream_t st, std::string* err) {
+  const bool var = softcap > 0.f || window > 0;
+  if (hd == 128)
+    return var ? launch_attn_tc<128, true>(c, q, k, v, o, B, start_pos, H, Hkv, softcap, window,
+                                           st, err)
+               : launch_attn_tc<128, false>(c, q, k, v, o, B, start_pos, H, Hkv, 0.f, 0, st, err);
+  return var ? launch_attn_tc<64, true>(c, q, k, v, o, B, start_pos, H, Hkv, softcap, window, st,
+                                        err)
+             : launch_attn_tc<64, false>(c, q, k, v, o, B, start_pos, H, Hkv, 0.f, 0, st, err);
 }
 
 }  // namespace pds

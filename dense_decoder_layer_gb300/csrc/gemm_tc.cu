@@ -73,7 +73,10 @@ namespace {
 #define PDS_GEMM_TRACE_HOOK(cta, point) ((void)0)
 #endif
 
-enum EpiKind { kEpiPlain = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiQkv = 3 };
+// kEpiQkv is the fast QKV epilogue (Neox over the whole head, no extras);
+// kEpiQkvX the general one (biases, q/k head norms, Norm layout, partial
+// rotation).
+enum EpiKind { kEpiPlain = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiQkv = 3, kEpiQkvX = 4 };
 
 constexpr int BM = 128;
 constexpr int BK = 64;
@@ -312,7 +315,8 @@ __host__ __device__ constexpr int owned_chunks() {
 }
 template <int BN, int EPI>
 __device__ __forceinline__ bool chunk_exists(const GemmArgs& g, int nt, int j) {
-  if constexpr (EPI == kEpiQkv) return nt * BN + j * 32 < g.qkv.q_width + 2 * g.qkv.kv_width;
+  if constexpr (EPI == kEpiQkv || EPI == kEpiQkvX)
+    return nt * BN + j * 32 < g.qkv.q_width + 2 * g.qkv.kv_width;
   return true;
 }
 
@@ -341,6 +345,133 @@ __device__ __forceinline__ void rope_prefetch(const GemmArgs& g, int nt, int ch,
   const float2* cs = rope_row(g, m);
 #pragma unroll
   for (int i = 0; i < 32; ++i) rr.v[i] = ld_rope(cs + static_cast<size_t>(i) * e.rope_ld);
+}
+
+// 16 floats of a device vector (16-byte aligned: four float4 loads).
+__device__ __forceinline__ void ld_f32x16(const float* p, float (&v)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 t = __ldg(reinterpret_cast<const float4*>(p) + q);
+    v[4 * q] = t.x;
+    v[4 * q + 1] = t.y;
+    v[4 * q + 2] = t.z;
+    v[4 * q + 3] = t.w;
+  }
+}
+
+// The general QKV epilogue of this thread's 128 columns (row `row`, column
+// half `ch`): t = r * acc + bias; for q and k every head becomes
+// t / sqrt(mean(t^2) + eps) * gain when it has a norm gain, then its first
+// rot_dim channels turn in pairs (Neox: (i, i + rot_dim/2); Norm: (2i, 2i+1))
+// by the (cos, sin) * mscale of the table; v rows are t.  Values are made
+// 16 columns at a time from TMEM (a rotated piece also makes its partner
+// piece) and stored through the warp's staging rows, 32 columns at a time.
+template <int BN>
+__device__ __forceinline__ void qkv_general_epilogue(const GemmArgs& g, uint32_t taddr, int mt,
+                                                     int nt, int row, int ch, int lane, float r,
+                                                     const Stage& st) {
+  const QkvEpilogue& e = g.qkv;
+  const int m = mt * BM + row;
+  const int m0w = mt * BM + (row & ~31);
+  const int rows = max(0, min(32, g.M - m0w));
+  const int c0 = nt * BN + ch * 128;  // first of this thread's 128 columns of [q | k | v]
+  if (c0 >= e.q_width + 2 * e.kv_width) return;
+  const int blk = c0 < e.q_width ? 0 : (c0 < e.q_width + e.kv_width ? 1 : 2);
+  const int cb = c0 - (blk == 0 ? 0 : (blk == 1 ? e.q_width : e.q_width + e.kv_width));
+  uint16_t* dst = blk == 0 ? e.q + static_cast<size_t>(m0w) * e.q_width + cb
+                           : (blk == 1 ? e.k_cache : e.v_cache) +
+                                 static_cast<size_t>(e.start_pos + m0w) * e.kv_width + cb;
+  const size_t ld = blk == 0 ? e.q_width : e.kv_width;
+  const float* bias = e.bias[blk];
+  const uint32_t tcol = taddr + static_cast<uint32_t>(ch * 128);
+  // r * acc + bias of columns cc .. cc + 15 (of the 128)
+  auto base16 = [&](int cc, float (&v)[16]) {
+    sm100::tmem_load16(tcol + cc, v);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] *= r;
+    if (bias) {
+      float b[16];
+      ld_f32x16(bias + cb + cc, b);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] += b[k];
+    }
+  };
+  auto store32 = [&](int cc, const float (&lo)[16], const float (&hi)[16]) {
+    stage_bf16(st, lane, 0, lo);
+    stage_bf16(st, lane, 2, hi);
+    flush_bf16(st, 0, dst + cc, ld, rows, lane);
+  };
+  if (blk == 2) {
+#pragma unroll 1
+    for (int cc = 0; cc < 128; cc += 32) {
+      float lo[16], hi[16];
+      base16(cc, lo);
+      base16(cc + 16, hi);
+      store32(cc, lo, hi);
+    }
+    return;
+  }
+  const int hd = e.head_dim, R = e.rot_dim, half = R / 2;
+  const float* gain = e.norm[blk];
+  const float2* cs = rope_row(g, m);
+#pragma unroll 1
+  for (int hb = 0; hb < 128; hb += hd) {  // heads of these 128 columns
+    float scale = 1.f;
+    if (gain) {
+      float ss = 0.f;
+#pragma unroll 1
+      for (int cc = hb; cc < hb + hd; cc += 16) {
+        float v[16];
+        base16(cc, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) ss = fmaf(v[k], v[k], ss);
+      }
+      scale = rsqrtf(ss / static_cast<float>(hd) + e.rs.eps);
+    }
+    // channels ic .. ic + 15 of the head, after the head norm
+    auto val16 = [&](int ic, float (&v)[16]) {
+      base16(hb + ic, v);
+      if (gain) {
+        float gv[16];
+        ld_f32x16(gain + ic, gv);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = v[k] * scale * gv[k];
+      }
+    };
+    // the 16 output channels from ic on
+    auto out16 = [&](int ic, float (&o)[16]) {
+      if (ic >= R) {
+        val16(ic, o);
+      } else if (e.rope_layout == PDS_ROPE_NORM) {
+        val16(ic, o);
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          const float2 sc = ld_rope(cs + static_cast<size_t>((ic + k) >> 1) * e.rope_ld);
+          const float u = o[k], w = o[k + 1];
+          o[k] = u * sc.x - w * sc.y;
+          o[k + 1] = u * sc.y + w * sc.x;
+        }
+      } else {
+        const bool first = ic < half;  // the pair's first channel: u cos - w sin
+        const int i0 = first ? ic : ic - half;
+        float u[16], w[16];
+        val16(i0, u);
+        val16(i0 + half, w);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 sc = ld_rope(cs + static_cast<size_t>(i0 + k) * e.rope_ld);
+          o[k] = first ? u[k] * sc.x - w[k] * sc.y : u[k] * sc.y + w[k] * sc.x;
+        }
+      }
+    };
+#pragma unroll 1
+    for (int ic = 0; ic < hd; ic += 32) {
+      float lo[16], hi[16];
+      out16(ic, lo);
+      out16(ic + 16, hi);
+      store32(hb + ic, lo, hi);
+    }
+  }
 }
 
 // The fused epilogue of one tile for this thread (row `row` of the tile,
@@ -444,6 +575,9 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
       flush_bf16(st, 0, e.act + static_cast<size_t>(m0w) * e.ffn + nt * 128 + jg * 32, e.ffn, rows,
                  lane);
     }
+  } else if constexpr (EPI == kEpiQkvX) {
+    static_assert(BN == 256, "the QKV tile holds whole heads in each 128-column half");
+    qkv_general_epilogue<BN>(g, taddr, mt, nt, row, ch, lane, r, st);
   } else {
     static_assert(BN == 256, "the QKV tile holds whole heads in each 128-column half");
     const QkvEpilogue& e = g.qkv;
@@ -1185,6 +1319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (EPI == kEpiQkv) {
         if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
         rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
+      } else if constexpr (EPI == kEpiQkvX) {
+        if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
       } else if constexpr (EPI == kEpiResid) {
         // the last tile's epilogue goes through shared memory and reads its gains there
         if (si.it >= si.end)
@@ -1707,7 +1843,10 @@ pds_status tc_gemm_qkv(TcContext& c, const uint16_t* A, const WeightRows& W, int
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
   for (int i = 0; i < 3; ++i)
     if ((rc = get_map(c, &maps.b[i], W.w[i], K, W.rows[i], err)) != PDS_OK) return rc;
-  return launch<256, kEpiQkv>(c, maps, g, st, err);
+  const bool general = e.rope_layout != PDS_ROPE_NEOX || e.rot_dim != e.head_dim || e.bias[0] ||
+                       e.bias[1] || e.bias[2] || e.norm[0] || e.norm[1];
+  return general ? launch<256, kEpiQkvX>(c, maps, g, st, err)
+                 : launch<256, kEpiQkv>(c, maps, g, st, err);
 }
 
 // ------------------------------------------------ no-allocation GEMM entry

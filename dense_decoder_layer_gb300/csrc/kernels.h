@@ -25,18 +25,24 @@ struct RowScale {
   float eps;
 };
 
-// QKV epilogue: scale rows, rotate q and k (NeoX half layout, table
-// [M, hd/2] of (cos, sin) at each row's position), write q and the new
-// cache rows.
+// QKV epilogue: scale rows, add the biases, RMSNorm every q / k head with
+// its gain, rotate q and k (table [rot_dim/2, M] of (cos, sin) * mscale at
+// each row's position), write q and the new cache rows.
 struct QkvEpilogue {
   RowScale rs;
-  const float2* rope;  // [hd/2, rope_ld]: channel i of row b at rope[i * rope_ld + b]
+  const float2* rope;  // [rot_dim/2, rope_ld]: pair i of row b at rope[i * rope_ld + b]
   int rope_ld;         // row stride of the table (the batch size)
   uint16_t* q;         // [M, H*hd]
   uint16_t* k_cache;   // [cap, Hkv*hd]; row b goes to row start_pos+b
   uint16_t* v_cache;
   int start_pos;
   int q_width, kv_width, head_dim;
+  // Variants (the general epilogue; the fast one serves Neox over the whole
+  // head with no extras).
+  int rope_layout;         // PDS_ROPE_NEOX / PDS_ROPE_NORM
+  int rot_dim;             // rotated channels per head
+  const float* bias[3];    // q [H*hd], k [Hkv*hd], v [Hkv*hd]; each may be null
+  const float* norm[2];    // q, k head norm gains [hd]; each may be null
 };
 
 // Residual epilogue: out = resid + acc (float32), and for a following

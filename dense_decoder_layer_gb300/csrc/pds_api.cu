@@ -75,8 +75,15 @@ Layout make_layout(const Plan& p, int B) {
   L.act = take(Bz * p.dims.ffn_dim * 2);
   L.rope = take(Bz * (p.dims.head_dim / 2) * 8);
   L.gemm_ws = take(gemm_workspace_bytes(p, B));
+  L.attn = off;
   L.total = off;
   return L;
+}
+
+size_t workspace_bytes(const Plan& p, int B, int s_max) {
+  const Layout L = make_layout(p, B);
+  return L.attn + align_up(tc_attention_scratch_bytes(B, s_max, p.dims.n_heads,
+                                                      p.dims.head_dim), 256);
 }
 
 }  // namespace pds
@@ -109,11 +116,40 @@ pds_status pds_plan_create(const pds_dims* dims, pds_plan** out) {
     return fail(PDS_DECLINED, "declined: d_model and ffn_dim must be multiples of 128");
   if ((d.n_heads * d.head_dim) % 128 != 0 || (d.n_kv_heads * d.head_dim) % 128 != 0)
     return fail(PDS_DECLINED, "declined: n_heads*head_dim and n_kv_heads*head_dim must be multiples of 128");
+  // run-wide RoPE and attention options
+  if (d.rope_layout != PDS_ROPE_NEOX && d.rope_layout != PDS_ROPE_NORM)
+    return fail(PDS_EINVAL, "pds_plan_create: rope_layout must be PDS_ROPE_NEOX or PDS_ROPE_NORM");
+  if (d.rot_dim < 0 || d.rot_dim > d.head_dim || d.rot_dim % 2)
+    return fail(PDS_EINVAL, "pds_plan_create: rot_dim must be 0 or even and <= head_dim");
+  const int rot = d.rot_dim ? d.rot_dim : d.head_dim;
+  if (rot % (d.rope_layout == PDS_ROPE_NEOX ? 32 : 16) != 0)
+    return fail(PDS_DECLINED, "declined: rot_dim must be a multiple of 32 (Neox) or 16 (Norm)");
+  if (!std::isfinite(d.rope_mscale) || d.rope_mscale < 0.f)
+    return fail(PDS_EINVAL, "pds_plan_create: rope_mscale must be 0 or > 0");
+  if (!std::isfinite(d.attn_softcap) || d.attn_softcap < 0.f)
+    return fail(PDS_EINVAL, "pds_plan_create: attn_softcap must be 0 or > 0");
+  if (d.window < 0) return fail(PDS_EINVAL, "pds_plan_create: window must be >= 0");
+  if (d.freq_factors)
+    for (int i = 0; i < rot / 2; ++i)
+      if (!(d.freq_factors[i] > 0.f) || !std::isfinite(d.freq_factors[i]))
+        return fail(PDS_EINVAL, "pds_plan_create: freq_factors must be finite and > 0");
   pds_plan* p = new (std::nothrow) pds_plan();
   if (!p) return fail(PDS_ENOMEM, "pds_plan_create: out of host memory");
   p->dims = d;
+  p->dims.freq_factors = nullptr;  // the caller's array is not kept
   p->q_width = d.n_heads * d.head_dim;
   p->kv_width = d.n_kv_heads * d.head_dim;
+  p->rope_layout = d.rope_layout;
+  p->rot_dim = rot;
+  // omega_i = theta^(-2i/rot_dim) / freq_factors[i], in float64
+  // (cuda_prefill.rs, LayerRopeCuda: theta, freq_factors, rot_dim)
+  p->omega.resize(rot / 2);
+  for (int i = 0; i < rot / 2; ++i)
+    p->omega[i] = std::pow(static_cast<double>(d.rope_theta), -2.0 * i / rot) /
+                  (d.freq_factors ? static_cast<double>(d.freq_factors[i]) : 1.0);
+  p->rope_mscale = d.rope_mscale > 0.f ? d.rope_mscale : 1.0f;
+  p->attn_softcap = d.attn_softcap;
+  p->window = d.window;
   const char* g = std::getenv("PDS_GRAPH");
   p->graphs = !(g && std::strcmp(g, "0") == 0);
   // The plan's device state, on the current device, once the shape is
@@ -139,9 +175,9 @@ void pds_plan_destroy(pds_plan* plan) {
   delete plan;
 }
 
-size_t pds_workspace_bytes(const pds_plan* plan, int32_t max_batch) {
-  if (!plan || max_batch < 1) return 0;
-  return pds::make_layout(*plan, max_batch).total;
+size_t pds_workspace_bytes(const pds_plan* plan, int32_t max_batch, int32_t max_start_pos) {
+  if (!plan || max_batch < 1 || max_start_pos < 0) return 0;
+  return pds::workspace_bytes(*plan, max_batch, max_start_pos);
 }
 
 static pds_status check_call(pds_plan* plan, const pds_layer* layers, uint16_t* const* kc,
@@ -158,7 +194,7 @@ static pds_status check_call(pds_plan* plan, const pds_layer* layers, uint16_t* 
   if (!ws) return fail(PDS_EINVAL, "workspace is NULL");
   if (!aligned16(ws)) return fail(PDS_EINVAL, "workspace is not 16-byte aligned");
   if (ws_bytes < pds::make_layout(*plan, B).total)
-    return fail(PDS_EINVAL, "workspace is smaller than pds_workspace_bytes(plan, batch)");
+    return fail(PDS_EINVAL, "workspace is smaller than pds_workspace_bytes(plan, batch, 0)");
   if (device_io && (!aligned16(in) || !aligned16(out)))
     return fail(PDS_EINVAL, "device hidden_in / hidden_out not 16-byte aligned");
   for (int l = 0; l < plan->dims.n_layers; ++l) {
@@ -170,6 +206,11 @@ static pds_status check_call(pds_plan* plan, const pds_layer* layers, uint16_t* 
       if (!aligned16(q))
         return fail(PDS_EINVAL, "layer " + std::to_string(l) + ": pointer not 16-byte aligned");
     }
+    for (const void* q : {(const void*)w.q_bias, (const void*)w.k_bias, (const void*)w.v_bias,
+                          (const void*)w.q_norm, (const void*)w.k_norm})
+      if (q && !aligned16(q))
+        return fail(PDS_EINVAL,
+                    "layer " + std::to_string(l) + ": extra (bias / norm) not 16-byte aligned");
   }
   // Fault injection for the callers' failure handling: the call is admitted,
   // then fails as a launch would, before any device work.
@@ -189,8 +230,8 @@ pds_status pds_prefill_dense_stack_device(pds_plan* plan, const pds_layer* layer
   if (st != PDS_OK) return st;
   std::string err;
   st = pds::run_stack(*plan, layers, k_cache, v_cache, start_pos, batch, hidden_in_dev,
-                          hidden_out_dev, static_cast<char*>(workspace),
-                          static_cast<cudaStream_t>(stream), &err);
+                      hidden_out_dev, static_cast<char*>(workspace), workspace_bytes,
+                      static_cast<cudaStream_t>(stream), &err);
   if (st != PDS_OK) return fail(st, err);
   return PDS_OK;
 }
@@ -212,7 +253,7 @@ pds_status pds_prefill_dense_stack(pds_plan* plan, const pds_layer* layers,
     return fail(PDS_ELAUNCH, std::string("upload of hidden_in: ") + cudaGetErrorString(ce));
   std::string err;
   st = pds::run_stack(*plan, layers, k_cache, v_cache, start_pos, batch, xdev, xdev,
-                          static_cast<char*>(workspace), s, &err);
+                      static_cast<char*>(workspace), workspace_bytes, s, &err);
   if (st != PDS_OK) return fail(st, err);
   ce = cudaMemcpyAsync(hidden_out, xdev, bytes, cudaMemcpyDeviceToHost, s);
   if (ce != cudaSuccess)
@@ -312,19 +353,31 @@ pds_status pds_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* W, float* C,
   return PDS_OK;
 }
 
+size_t pds_attention_workspace_bytes(int32_t batch, int32_t start_pos, int32_t n_heads,
+                                     int32_t head_dim) {
+  if (batch < 1 || start_pos < 0 || n_heads < 1 || (head_dim != 64 && head_dim != 128)) return 0;
+  return pds::tc_attention_scratch_bytes(batch, start_pos, n_heads, head_dim);
+}
+
 pds_status pds_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
                          int32_t batch, int32_t start_pos, int32_t n_heads, int32_t n_kv_heads,
-                         int32_t head_dim, void* stream) {
+                         int32_t head_dim, float softcap, int32_t window, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o) return fail(PDS_EINVAL, "pds_attention: NULL operand");
   if (batch < 1 || start_pos < 0 || n_heads < 1 || n_kv_heads < 1)
     return fail(PDS_EINVAL, "pds_attention: bad size");
+  if (!(softcap >= 0.f) || !std::isfinite(softcap) || window < 0)
+    return fail(PDS_EINVAL, "pds_attention: softcap and window must be >= 0");
   if (n_heads % n_kv_heads != 0 || (head_dim != 64 && head_dim != 128))
     return fail(PDS_DECLINED, "declined: pds_attention needs H % Hkv == 0 and hd in {64, 128}");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (workspace && !aligned16(workspace)))
     return fail(PDS_EINVAL, "pds_attention: operand not 16-byte aligned");
+  if (!workspace) workspace_bytes = 0;
   std::string err;
   pds_status st = pds::run_attention(q, k, v, o, batch, start_pos, n_heads, n_kv_heads, head_dim,
-                                     static_cast<cudaStream_t>(stream), &err);
+                                     softcap, window, static_cast<char*>(workspace),
+                                     workspace_bytes, static_cast<cudaStream_t>(stream), &err);
   if (st != PDS_OK) return fail(st, err);
   return PDS_OK;
 }

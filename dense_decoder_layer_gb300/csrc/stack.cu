@@ -191,7 +191,7 @@ pds_status plan_sync(Plan& p, cudaStream_t st, std::string* err) {
 
 pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
                          uint16_t* const* v_cache, int s, int B, const float* x_in, float* x_out,
-                         char* ws, cudaStream_t st, std::string* err) {
+                         char* ws, size_t ws_bytes, cudaStream_t st, std::string* err) {
   pds_status rc = check_device_state(p, err);
   if (rc != PDS_OK) return rc;
   const pds_dims& D = p.dims;
@@ -229,13 +229,11 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
     if (m) cudaEventRecord(m->stop, st);
   };
 
-  // RoPE frequencies in float64: omega_i = theta^(-2i/hd) (cuda_prefill.rs,
-  // LayerRopeCuda: theta, rot_dim = head_dim)
+  // the plan's float64 angular frequencies of the rotated pairs
   RopeFreqs rf{};
-  rf.n_pairs = hd / 2;
-  rf.mscale = 1.0f;
-  for (int i = 0; i < rf.n_pairs; ++i)
-    rf.omega[i] = std::pow(static_cast<double>(D.rope_theta), -2.0 * i / hd);
+  rf.n_pairs = p.rot_dim / 2;
+  rf.mscale = p.rope_mscale;
+  for (int i = 0; i < rf.n_pairs; ++i) rf.omega[i] = p.omega[i];
 
   Plan::Mark* mk = mark(PDS_KERNEL_PREP);
   launch_rope_table(rope, B, s, rf, st);
@@ -250,6 +248,8 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
   tc.ws_bytes = gemm_workspace_bytes(p, B);
   tc.maps = p.maps;
   tc.pdl = true;
+  tc.attn_ws = ws + lay.attn;
+  tc.attn_ws_bytes = ws_bytes > lay.attn ? ws_bytes - lay.attn : 0;
   {
     // stream-K tile counters start at zero; every GEMM leaves them at zero
     const size_t part = tc_gemm_scratch_bytes(B, 0);
@@ -277,6 +277,13 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
     qe.q_width = p.q_width;
     qe.kv_width = p.kv_width;
     qe.head_dim = hd;
+    qe.rope_layout = p.rope_layout;
+    qe.rot_dim = p.rot_dim;
+    qe.bias[0] = w.q_bias;
+    qe.bias[1] = w.k_bias;
+    qe.bias[2] = w.v_bias;
+    qe.norm[0] = w.q_norm;
+    qe.norm[1] = w.k_norm;
     WeightRows wqkv{{w.wq, w.wk, w.wv}, {p.q_width, p.kv_width, p.kv_width}, 3};
 
     ResidEpilogue oe{x_cur, Hs, w.ffn_norm_w, A, ss_ffn};
@@ -289,8 +296,8 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
     done(mk);
     if (rc != PDS_OK) return rc;
     mk = mark(PDS_KERNEL_ATTN);
-    rc = tc_attention(tc, Q, k_cache[l], v_cache[l], O, B, s, D.n_heads, D.n_kv_heads, hd, st,
-                      err);
+    rc = tc_attention(tc, Q, k_cache[l], v_cache[l], O, B, s, D.n_heads, D.n_kv_heads, hd,
+                      p.attn_softcap, p.window, st, err);
     done(mk);
     if (rc != PDS_OK) return rc;
     mk = mark(PDS_KERNEL_WO);
@@ -311,24 +318,27 @@ pds_status enqueue_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_ca
 
 pds_status run_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
                      uint16_t* const* v_cache, int s, int B, const float* x_in, float* x_out,
-                     char* ws, cudaStream_t st, std::string* err) {
+                     char* ws, size_t ws_bytes, cudaStream_t st, std::string* err) {
   if (!p.graphs || p.timing)
-    return enqueue_stack(p, layers, k_cache, v_cache, s, B, x_in, x_out, ws, st, err);
+    return enqueue_stack(p, layers, k_cache, v_cache, s, B, x_in, x_out, ws, ws_bytes, st, err);
   pds_status rc = check_device_state(p, err);
   if (rc != PDS_OK) return rc;
   std::vector<uintptr_t> key;
-  key.reserve(8 + 11 * p.dims.n_layers);
+  key.reserve(8 + 16 * p.dims.n_layers);
   key.push_back(static_cast<uintptr_t>(s));
   key.push_back(static_cast<uintptr_t>(B));
   key.push_back(reinterpret_cast<uintptr_t>(x_in));
   key.push_back(reinterpret_cast<uintptr_t>(x_out));
   key.push_back(reinterpret_cast<uintptr_t>(ws));
+  key.push_back(static_cast<uintptr_t>(ws_bytes));
   for (int l = 0; l < p.dims.n_layers; ++l) {
     const pds_layer& w = layers[l];
     for (const void* q : {(const void*)w.attn_norm_w, (const void*)w.ffn_norm_w,
                           (const void*)w.wq, (const void*)w.wk, (const void*)w.wv,
                           (const void*)w.wo, (const void*)w.w_gate, (const void*)w.w_up,
-                          (const void*)w.w_down, (const void*)k_cache[l], (const void*)v_cache[l]})
+                          (const void*)w.w_down, (const void*)k_cache[l], (const void*)v_cache[l],
+                          (const void*)w.q_bias, (const void*)w.k_bias, (const void*)w.v_bias,
+                          (const void*)w.q_norm, (const void*)w.k_norm})
       key.push_back(reinterpret_cast<uintptr_t>(q));
   }
   Plan::Graph* hit = nullptr;
@@ -340,7 +350,8 @@ pds_status run_stack(Plan& p, const pds_layer* layers, uint16_t* const* k_cache,
       *err = std::string("graph capture start: ") + cudaGetErrorString(ce);
       return PDS_ELAUNCH;
     }
-    rc = enqueue_stack(p, layers, k_cache, v_cache, s, B, x_in, x_out, ws, p.capture_stream, err);
+    rc = enqueue_stack(p, layers, k_cache, v_cache, s, B, x_in, x_out, ws, ws_bytes,
+                       p.capture_stream, err);
     cudaGraph_t graph = nullptr;
     ce = cudaStreamEndCapture(p.capture_stream, &graph);
     if (rc != PDS_OK || ce != cudaSuccess) {
@@ -408,12 +419,15 @@ pds_status plan_kernel_times(Plan& p, cudaStream_t st, pds_kernel_times* out, bo
 }
 
 pds_status run_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
-                         int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
-                         std::string* err) {
+                         int B, int start_pos, int H, int Hkv, int hd, float softcap, int window,
+                         char* ws, size_t ws_bytes, cudaStream_t st, std::string* err) {
   TcContext tc{};
   tc.num_sms = current_num_sms();
+  tc.attn_ws = ws;
+  tc.attn_ws_bytes = ws_bytes;
   if (!(tc.status = component_status(err))) return PDS_ELAUNCH;
-  pds_status rc = tc_attention(tc, q, k, v, o, B, start_pos, H, Hkv, hd, st, err);
+  pds_status rc =
+      tc_attention(tc, q, k, v, o, B, start_pos, H, Hkv, hd, softcap, window, st, err);
   if (rc == PDS_OK) rc = check_launch("attention", err);
   return rc;
 }

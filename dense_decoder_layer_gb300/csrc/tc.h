@@ -20,6 +20,8 @@ struct TcContext {
   uint32_t* status = nullptr;  // device status word (bounded waits)
   char* ws = nullptr;          // GEMM scratch: stream-K partial tiles, tile counters
   size_t ws_bytes = 0;
+  char* attn_ws = nullptr;     // attention scratch: partial rows of chunked key ranges
+  size_t attn_ws_bytes = 0;    // 0: no chunked mode
   TmapCache* maps = nullptr;   // optional
   bool pdl = false;            // launch with programmatic stream serialization
 };
@@ -63,8 +65,15 @@ int kernel_max_clusters(const void* fn, const cudaLaunchConfig_t& cfg, int cs);
 pds_status tc_map_bf16(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner,
                        uint64_t outer, uint32_t box_rows, std::string* err);
 // GQA causal attention on the tcgen05 tensor cores (head_dim 64 or 128).
+// Attention scratch: bytes per unit of the chunked mode, and the most a call
+// with batch B over an s-row prefix can use (chunked key ranges are used
+// only as far as the scratch given in TcContext holds them).
+size_t tc_attention_unit_bytes(int hd);
+size_t tc_attention_scratch_bytes(int B, int s, int H, int hd);
+// softcap > 0 caps the scaled scores (softcap * tanh(z / softcap)); window
+// > 0 lets the row at position p see keys p - window < j <= p only.
 pds_status tc_attention(TcContext& c, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                        uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, cudaStream_t st,
-                        std::string* err);
+                        uint16_t* o, int B, int start_pos, int H, int Hkv, int hd, float softcap,
+                        int window, cudaStream_t st, std::string* err);
 
 }  // namespace pds

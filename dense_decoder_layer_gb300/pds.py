@@ -28,18 +28,26 @@ class PdsError(RuntimeError):
         self.status = status
 
 
+PDS_ROPE_NEOX, PDS_ROPE_NORM = 0, 1
+
+
 class pds_dims(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32),
                 ("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("ffn_dim", ctypes.c_int32),
-                ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+                ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("rope_layout", ctypes.c_int32), ("rot_dim", ctypes.c_int32),
+                ("freq_factors", ctypes.POINTER(ctypes.c_float)),
+                ("rope_mscale", ctypes.c_float), ("attn_softcap", ctypes.c_float),
+                ("window", ctypes.c_int32)]
 
 
 LAYER_FIELDS = ("attn_norm_w", "ffn_norm_w", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+EXTRA_FIELDS = ("q_bias", "k_bias", "v_bias", "q_norm", "k_norm")
 
 
 class pds_layer(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_FIELDS]
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_FIELDS + EXTRA_FIELDS]
 
 
 KERNEL_KINDS = ("prep", "qkv", "attn", "wo", "gateup", "down")
@@ -70,7 +78,7 @@ def load() -> ctypes.CDLL:
     sig = {
         "pds_plan_create": (st, [ctypes.POINTER(pds_dims), ctypes.POINTER(ctypes.c_void_p)]),
         "pds_plan_destroy": (None, [vp]),
-        "pds_workspace_bytes": (sz, [vp, i32]),
+        "pds_workspace_bytes": (sz, [vp, i32, i32]),
         "pds_prefill_dense_stack": (st, [vp, ctypes.POINTER(pds_layer), pp, pp, i32, i32, i32,
                                          vp, vp, vp, sz, vp]),
         "pds_prefill_dense_stack_device": (st, [vp, ctypes.POINTER(pds_layer), pp, pp, i32, i32,
@@ -80,7 +88,9 @@ def load() -> ctypes.CDLL:
         "pds_gemm_bf16": (st, [vp, vp, vp, i32, i32, i32, vp, sz, vp]),
         "pds_gemm_workspace_bytes": (sz, [i32, i32]),
         "pds_gemm_bf16_noalloc": (st, [vp, vp, vp, i32, i32, i32, vp]),
-        "pds_attention": (st, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+        "pds_attention": (st, [vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                               vp, sz, vp]),
+        "pds_attention_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "pds_plan_set_timing": (st, [vp, i32]),
         "pds_selftest_stuck_wait": (st, [ctypes.c_uint32, vp]),
         "pds_component_sync": (st, [vp]),
@@ -131,8 +141,8 @@ def pds_plan_destroy(plan) -> None:
     load().pds_plan_destroy(plan)
 
 
-def pds_workspace_bytes(plan, max_batch: int) -> int:
-    return load().pds_workspace_bytes(plan, max_batch)
+def pds_workspace_bytes(plan, max_batch: int, max_start_pos: int = 0) -> int:
+    return load().pds_workspace_bytes(plan, max_batch, max_start_pos)
 
 
 def _layer_array(layers):
@@ -140,8 +150,8 @@ def _layer_array(layers):
         return layers
     arr = (pds_layer * len(layers))()
     for i, l in enumerate(layers):
-        for n in LAYER_FIELDS:
-            setattr(arr[i], n, l[n])
+        for n in LAYER_FIELDS + EXTRA_FIELDS:
+            setattr(arr[i], n, l.get(n))
     return arr
 
 
@@ -182,9 +192,16 @@ def pds_gemm_bf16_noalloc(A, W, C, M, N, K, stream) -> None:
     check(load().pds_gemm_bf16_noalloc(A, W, C, M, N, K, stream))
 
 
-def pds_attention(q, k, v, o, batch, start_pos, n_heads, n_kv_heads, head_dim, stream) -> None:
+def pds_attention(q, k, v, o, batch, start_pos, n_heads, n_kv_heads, head_dim, stream,
+                  softcap: float = 0.0, window: int = 0, workspace=None,
+                  workspace_bytes: int = 0) -> None:
     check(load().pds_attention(q, k, v, o, batch, start_pos, n_heads, n_kv_heads, head_dim,
+                               softcap, window, workspace, workspace_bytes if workspace else 0,
                                stream))
+
+
+def pds_attention_workspace_bytes(batch, start_pos, n_heads, head_dim) -> int:
+    return load().pds_attention_workspace_bytes(batch, start_pos, n_heads, head_dim)
 
 
 def pds_plan_set_timing(plan, enable: bool) -> None:
@@ -210,3 +227,24 @@ def pds_component_sync(stream) -> int:
     if st not in (PDS_OK, PDS_ETIMEOUT):
         raise PdsError(st, last_error())
     return st
+
+
+def make_dims(dims, variant=None, freq_factors=None) -> pds_dims:
+    """``pds_dims`` of any object with the model fields (n_layers, d_model,
+    n_heads, n_kv_heads, head_dim, ffn_dim, rope_theta, rms_eps) and of an
+    optional variant (rope_layout "neox"/"norm", rot_dim, rope_mscale,
+    attn_softcap, window); ``freq_factors`` is a float32 array or None.  The
+    returned struct keeps the factors' C array alive (``_keep``)."""
+    pd = pds_dims(dims.n_layers, dims.d_model, dims.n_heads, dims.n_kv_heads, dims.head_dim,
+                  dims.ffn_dim, dims.rope_theta, dims.rms_eps)
+    if variant is not None:
+        pd.rope_layout = PDS_ROPE_NORM if variant.rope_layout == "norm" else PDS_ROPE_NEOX
+        pd.rot_dim = int(variant.rot_dim or 0)
+        pd.rope_mscale = float(variant.rope_mscale or 0.0)
+        pd.attn_softcap = float(variant.attn_softcap or 0.0)
+        pd.window = int(variant.window or 0)
+    if freq_factors is not None:
+        arr = (ctypes.c_float * len(freq_factors))(*[float(f) for f in freq_factors])
+        pd.freq_factors = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+        pd._keep = arr
+    return pd

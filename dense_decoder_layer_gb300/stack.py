@@ -14,6 +14,7 @@ import torch
 from . import pds
 
 LAYER_FIELDS = pds.LAYER_FIELDS
+EXTRA_FIELDS = pds.EXTRA_FIELDS
 # pds_layer field -> tensor name of a drawn layer (synth.LAYER_TENSORS)
 SYNTH_NAMES = {"attn_norm_w": "attn_norm", "ffn_norm_w": "ffn_norm"}
 
@@ -27,18 +28,20 @@ def _bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
 class DenseStack:
     """A run of ``n_layers`` dense layers on one GPU, with its caches.
 
-    ``dims`` is any object with the fields of ``pds_dims`` (n_layers,
-    d_model, n_heads, n_kv_heads, head_dim, ffn_dim, rope_theta, rms_eps).
+    ``dims`` is any object with the model fields of ``pds_dims`` (n_layers,
+    d_model, n_heads, n_kv_heads, head_dim, ffn_dim, rope_theta, rms_eps);
+    ``variant`` optionally gives the run-wide RoPE / attention options
+    (rope_layout, rot_dim, rope_mscale, attn_softcap, window) and
+    ``freq_factors`` the RoPE frequency factors.
     """
 
-    def __init__(self, dims, cache_capacity: int, max_batch: int, device="cuda"):
+    def __init__(self, dims, cache_capacity: int, max_batch: int, device="cuda", variant=None,
+                 freq_factors=None):
         self.dims = dims
         self.device = torch.device(device)
         self.cache_capacity = int(cache_capacity)
         self.max_batch = int(max_batch)
-        self.plan = pds.pds_plan_create(pds.pds_dims(
-            dims.n_layers, dims.d_model, dims.n_heads, dims.n_kv_heads, dims.head_dim,
-            dims.ffn_dim, dims.rope_theta, dims.rms_eps))
+        self.plan = pds.pds_plan_create(pds.make_dims(dims, variant, freq_factors))
         kvw = dims.n_kv_heads * dims.head_dim
         L = dims.n_layers
         self.k_cache = [torch.zeros(self.cache_capacity, kvw, dtype=torch.bfloat16,
@@ -47,7 +50,9 @@ class DenseStack:
         # the C arrays of pointers are built once, not on every call
         self._k_ptrs = pds._ptrs([t.data_ptr() for t in self.k_cache])
         self._v_ptrs = pds._ptrs([t.data_ptr() for t in self.v_cache])
-        self.ws_bytes = pds.pds_workspace_bytes(self.plan, self.max_batch)
+        # room for the attention's chunked key ranges up to the cache's capacity
+        self.ws_bytes = pds.pds_workspace_bytes(self.plan, self.max_batch,
+                                                max(0, self.cache_capacity - 1))
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.weights = []
         self._layer_ptrs = []
@@ -67,24 +72,28 @@ class DenseStack:
     # ------------------------------------------------------------ weights
     def load_layers(self, layers) -> None:
         """``layers``: per-layer dicts of numpy arrays (bf16 bits uint16 for
-        matrices, float32 for the gains), as :func:`synth.draw_layer` makes."""
+        matrices, float32 for the gains and the optional extras), as
+        :func:`synth.draw_workload` makes."""
         self.weights, self._layer_ptrs = [], []
         for l in layers:
             t = {}
-            for n in LAYER_FIELDS:
-                a = l[n] if n in l else l[SYNTH_NAMES[n]]
+            for n in LAYER_FIELDS + EXTRA_FIELDS:
+                a = l.get(n, l.get(SYNTH_NAMES.get(n, ""), None))
+                if a is None:
+                    continue
                 if a.dtype == np.uint16:
                     t[n] = _bf16_tensor(a, self.device)
                 else:
                     t[n] = torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(self.device)
             self.weights.append(t)
-            self._layer_ptrs.append({n: t[n].data_ptr() for n in LAYER_FIELDS})
+            self._layer_ptrs.append({n: t[n].data_ptr() for n in t})
         self._layers_c = pds._layer_array(self._layer_ptrs)
 
     def set_layer_tensors(self, layers) -> None:
         """Use device tensors the caller already holds (dicts field -> tensor)."""
         self.weights = list(layers)
-        self._layer_ptrs = [{n: l[n].data_ptr() for n in LAYER_FIELDS} for l in layers]
+        self._layer_ptrs = [{n: l[n].data_ptr() for n in LAYER_FIELDS + EXTRA_FIELDS if n in l}
+                            for l in layers]
         self._layers_c = pds._layer_array(self._layer_ptrs)
 
     def load_prefix(self, prefix_k, prefix_v) -> None:

@@ -54,12 +54,31 @@ typedef enum pds_status {
   PDS_ENOMEM = 5    /* a host or plan-internal device allocation failed    */
 } pds_status;
 
+/* RoPE layouts (cuda_prefill.rs, RopeLayoutCuda). */
+enum {
+  PDS_ROPE_NEOX = 0, /* pair i = channels (i, i + rot_dim/2)  */
+  PDS_ROPE_NORM = 1  /* pair i = channels (2i, 2i + 1)        */
+};
+
 /*
- * Model dimensions of the run (cuda_prefill.rs, PrefillParams: n_heads,
- * n_kv_heads, head_dim, rms_eps; LayerRopeCuda: theta).  RoPE is the NeoX
- * layout over the whole head with omega_i = rope_theta^(-2i/head_dim); no
- * frequency factors, no attention-factor scaling, no softcap, no window;
- * the attention scale is 1/sqrt(head_dim).  One rms_eps serves both norms.
+ * Model dimensions and the run-wide options (cuda_prefill.rs,
+ * PrefillParams: n_heads, n_kv_heads, head_dim, rms_eps, attn_softcap,
+ * window; LayerRopeCuda: theta, freq_factors, rot_dim, layout, mscale).
+ * One rms_eps serves both norms (and the q/k norms); the attention scale
+ * is 1/sqrt(head_dim).  Every layer of a run shares the RoPE description,
+ * the softcap and the window (a model whose layers differ in them is run as
+ * several runs).
+ *
+ * RoPE: the first rot_dim channels of every q and k head form rot_dim/2
+ * pairs (see the layouts); pair i turns by the angle p * omega_i at
+ * position p, omega_i = rope_theta^(-2i/rot_dim) / freq_factors[i], and
+ * both channels of the pair are multiplied by rope_mscale; channels from
+ * rot_dim on pass unchanged.  Softcap: a scaled score z becomes
+ * attn_softcap * tanh(z / attn_softcap).  Window: the row at position p
+ * sees the keys j with p - window < j <= p.
+ *
+ * A zero-initialised tail (from rope_layout on) means: Neox over the whole
+ * head, no frequency factors, scale 1, no softcap, no window.
  */
 typedef struct pds_dims {
   int32_t n_layers;   /* L >= 1                                    */
@@ -70,12 +89,27 @@ typedef struct pds_dims {
   int32_t ffn_dim;    /* F: multiple of 128                        */
   float rope_theta;   /* > 0                                       */
   float rms_eps;      /* >= 0                                      */
+  int32_t rope_layout;        /* PDS_ROPE_NEOX or PDS_ROPE_NORM    */
+  int32_t rot_dim;            /* 0 (= head_dim), or a positive multiple of
+                                 32 (Neox) / 16 (Norm), <= head_dim */
+  const float* freq_factors;  /* host [rot_dim/2] > 0, or NULL (all 1);
+                                 copied by pds_plan_create          */
+  float rope_mscale;          /* 0 (= 1), or > 0                    */
+  float attn_softcap;         /* 0 (none), or > 0                   */
+  int32_t window;             /* 0 (none), or > 0 positions         */
 } pds_dims;
 
 /*
  * One layer's weights, all device pointers (cuda_prefill.rs,
  * PrefillDenseLayerCuda: attn_norm_w, ffn_norm_w, q, k, v, o, gate, up,
- * down).  The caller owns them; they are read, never written.
+ * down, and the attention extras of AttnExtrasCuda).  The caller owns
+ * them; they are read, never written.
+ *
+ * The extras are optional (NULL: absent), each on its own: a bias is added
+ * to its projection's output (after the attention norm's row scale); the
+ * q/k norm gains make every head of q / k an RMSNorm of itself,
+ * head / sqrt(mean(head^2) + rms_eps) * gain, after the bias and before
+ * RoPE.
  */
 typedef struct pds_layer {
   const float* attn_norm_w; /* [d]               */
@@ -87,6 +121,11 @@ typedef struct pds_layer {
   const uint16_t* w_gate;   /* [F, d]       bf16 */
   const uint16_t* w_up;     /* [F, d]       bf16 */
   const uint16_t* w_down;   /* [d, F]       bf16 */
+  const float* q_bias;      /* [H*hd]   or NULL  */
+  const float* k_bias;      /* [Hkv*hd] or NULL  */
+  const float* v_bias;      /* [Hkv*hd] or NULL  */
+  const float* q_norm;      /* [hd]     or NULL  */
+  const float* k_norm;      /* [hd]     or NULL  */
 } pds_layer;
 
 typedef struct pds_plan pds_plan;
@@ -123,12 +162,18 @@ pds_status pds_plan_create(const pds_dims* dims, pds_plan** out);
 void pds_plan_destroy(pds_plan* plan);
 
 /*
- * Bytes of device workspace a call with batch <= max_batch needs.  The
- * workspace holds the activations between kernels (never the weights or
- * the caches); its content on entry does not matter.  0 for a NULL plan or
- * max_batch < 1.
+ * Bytes of device workspace for calls with batch <= max_batch and
+ * start_pos <= max_start_pos.  The workspace holds the activations between
+ * kernels (never the weights or the caches); its content on entry does not
+ * matter.  A call needs at least pds_workspace_bytes(plan, batch, 0); what
+ * it is given beyond that holds the partial rows of long key ranges, which
+ * attention then spreads over all SMs in equal chunks (merged in a fixed
+ * order) as far as they fit.  So the schedule, and the rounding of the
+ * result, depends on the workspace size: the same inputs with the same
+ * workspace size give the same bits.  0 for a NULL plan, max_batch < 1 or
+ * max_start_pos < 0.
  */
-size_t pds_workspace_bytes(const pds_plan* plan, int32_t max_batch);
+size_t pds_workspace_bytes(const pds_plan* plan, int32_t max_batch, int32_t max_start_pos);
 
 /*
  * The prefill call, host in / host out (cuda_prefill.rs,
@@ -291,16 +336,31 @@ pds_status pds_gemm_bf16_noalloc(const uint16_t* A, const uint16_t* W, float* C,
 
 /*
  * GQA causal attention of B new query rows over a cache (cuda_prefill.rs,
- * PrefillParams: prefix_k/prefix_v, start_pos, attn_scale = 1/sqrt(hd)).
- *  q      bf16 [B, H, hd], already rotated (not pre-scaled).
- *  k, v   bf16 [>= start_pos+B, Hkv, hd]; rows [0, start_pos+B) are read.
- *  o      bf16 [B, H*hd]; row b attends rows j <= start_pos + b; query head
- *         h reads kv head h / (H/Hkv).
- * Fails with PDS_DECLINED for hd not in {64, 128} or H % Hkv != 0.
+ * PrefillParams: prefix_k/prefix_v, start_pos, attn_scale = 1/sqrt(hd),
+ * attn_softcap, window).
+ *  q        bf16 [B, H, hd], already rotated (not pre-scaled).
+ *  k, v     bf16 [>= start_pos+B, Hkv, hd]; rows [0, start_pos+B) are read.
+ *  o        bf16 [B, H*hd]; row b (position p = start_pos + b) attends rows
+ *           j <= p, and with window > 0 only p - window < j <= p; query head
+ *           h reads kv head h / (H/Hkv).
+ *  softcap  0 (none) or > 0: scaled scores z become softcap*tanh(z/softcap).
+ *  workspace, workspace_bytes  device scratch for long key ranges (see
+ *           pds_attention_workspace_bytes), or NULL and 0.
+ * Fails with PDS_DECLINED for hd not in {64, 128} or H % Hkv != 0, and with
+ * PDS_EINVAL for a negative softcap or window.
  */
 pds_status pds_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
                          int32_t batch, int32_t start_pos, int32_t n_heads, int32_t n_kv_heads,
-                         int32_t head_dim, void* stream);
+                         int32_t head_dim, float softcap, int32_t window, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes with which pds_attention can spread long key ranges over
+ * all SMs (its workspace argument; NULL / 0 also works, with long ranges
+ * then split over CTA pairs only).  0 for bad sizes.
+ */
+size_t pds_attention_workspace_bytes(int32_t batch, int32_t start_pos, int32_t n_heads,
+                                     int32_t head_dim);
 
 #ifdef __cplusplus
 }

@@ -16,6 +16,10 @@ shapes and the distributions, the generator choice is ours):
   rounded to bf16.  The K prefix is taken as already rotated (a rotation
   of an isotropic Gaussian pair is again an isotropic Gaussian pair, so
   drawing the rotated values directly gives the same distribution).
+* optional attention extras per layer (float32): q/k/v biases ~ N(0, 0.5^2),
+  q/k norm gains ``1 + 0.1*N(0,1)`` of ``[head_dim]``;
+* optional RoPE frequency factors ``1 + 3*U[0,1)`` per rotated pair
+  (float32), drawn once per workload.
 
 Every tensor has its own PCG64 stream, keyed by ``(seed, layer, tensor
 id)``, so tensors can be drawn in parallel threads and a subset of the
@@ -34,6 +38,12 @@ import numpy as np
 
 __all__ = [
     "Dims",
+    "Variant",
+    "NO_VARIANT",
+    "EXTRA_TENSORS",
+    "draw_extras",
+    "draw_freq_factors",
+    "variant_options",
     "CONFIGS",
     "LAYER_TENSORS",
     "bf16_round",
@@ -72,6 +82,23 @@ class Dims:
         return dataclasses.replace(self, **kw)
 
 
+@dataclasses.dataclass(frozen=True)
+class Variant:
+    """The optional parts of a run: attention extras (per layer) and the
+    RoPE / attention options (the same for every layer of the run)."""
+
+    extras: bool = False          # q/k/v biases and q/k norm gains in every layer
+    rope_layout: str = "neox"     # "neox" or "norm"
+    rot_dim: int = 0              # 0: the whole head
+    freq_factors: bool = False    # draw frequency factors
+    rope_mscale: float = 1.0
+    attn_softcap: float = 0.0     # 0: none
+    window: int = 0               # 0: none
+
+
+NO_VARIANT = Variant()
+
+
 # The workloads of the dense prefill stack, by what they are.
 CONFIGS = {
     "tiny": Dims(2, 256, 4, 2, 64, 768, 8, 0, 1.0e4),
@@ -79,11 +106,20 @@ CONFIGS = {
     "llama3.2-3b-pp512": Dims(28, 3072, 24, 8, 128, 8192, 512, 0, 5.0e5),
     "llama3.2-3b-pp512-prefix1536": Dims(28, 3072, 24, 8, 128, 8192, 512, 1536, 5.0e5),
     "llama3-8b-pp2048-prefix2048": Dims(32, 4096, 32, 8, 128, 14336, 2048, 2048, 5.0e5),
+    # decode steps against a resident 2048-row cache (the matvec regime)
+    "llama3.2-3b-decode-b1-ctx2048": Dims(28, 3072, 24, 8, 128, 8192, 1, 2048, 5.0e5),
+    "llama3.2-3b-decode-b8-ctx2048": Dims(28, 3072, 24, 8, 128, 8192, 8, 2048, 5.0e5),
+    # long cached prefixes (attention-dominated prefill)
+    "llama3.2-3b-pp512-prefix8192": Dims(28, 3072, 24, 8, 128, 8192, 512, 8192, 5.0e5),
+    "llama3.2-3b-pp512-prefix32768": Dims(28, 3072, 24, 8, 128, 8192, 512, 32768, 5.0e5),
 }
 
 # Tensor ids of one layer, in a fixed order (the id keys the stream).
 LAYER_TENSORS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
 _PREFIX_K, _PREFIX_V = 9, 10
+EXTRA_TENSORS = ("q_bias", "k_bias", "v_bias", "q_norm", "k_norm")
+_EXTRA_IDS = {n: 11 + i for i, n in enumerate(EXTRA_TENSORS)}
+_FREQ_FACTORS = 16
 _HIDDEN_LAYER = 0xFFFF
 
 
@@ -163,7 +199,40 @@ def draw_prefix(dims: Dims, layer: int, seed: int = 0):
     return out[0], out[1]
 
 
-def draw_workload(dims: Dims, seed: int = 0, threads: int | None = None):
+def draw_extras(dims: Dims, layer: int, seed: int = 0) -> dict:
+    """One layer's attention extras (float32): biases ``[H*hd]``/``[Hkv*hd]``
+    ~ N(0, 0.5^2) and q/k norm gains ``[hd]`` = 1 + 0.1*N(0,1)."""
+    shapes = {"q_bias": dims.q_width, "k_bias": dims.kv_width, "v_bias": dims.kv_width,
+              "q_norm": dims.head_dim, "k_norm": dims.head_dim}
+    out = {}
+    for n in EXTRA_TENSORS:
+        z = _rng(seed, layer, _EXTRA_IDS[n]).standard_normal(shapes[n], dtype=np.float32)
+        if n.endswith("_norm"):
+            out[n] = (np.float32(1.0) + np.float32(0.1) * z).astype(np.float32)
+        else:
+            out[n] = (np.float32(0.5) * z).astype(np.float32)
+    return out
+
+
+def draw_freq_factors(dims: Dims, variant: Variant, seed: int = 0):
+    """RoPE frequency factors ``1 + 3*U[0,1)`` per rotated pair (float32), or None."""
+    if not variant.freq_factors:
+        return None
+    pairs = (variant.rot_dim or dims.head_dim) // 2
+    u = _rng(seed, _HIDDEN_LAYER, _FREQ_FACTORS).random(pairs, dtype=np.float32)
+    return (np.float32(1.0) + np.float32(3.0) * u).astype(np.float32)
+
+
+def variant_options(dims: Dims, variant: Variant, seed: int = 0) -> dict:
+    """The run-wide options of a variant as keyword arguments (oracle names)."""
+    return dict(rope_layout=variant.rope_layout, rot_dim=variant.rot_dim or None,
+                freq_factors=draw_freq_factors(dims, variant, seed),
+                rope_mscale=variant.rope_mscale, attn_softcap=variant.attn_softcap or None,
+                window=variant.window or None)
+
+
+def draw_workload(dims: Dims, seed: int = 0, threads: int | None = None,
+                  variant: Variant = NO_VARIANT):
     """All inputs of one call.
 
     Returns ``(layers, prefix_k, prefix_v, hidden)`` with ``layers`` a list
@@ -177,4 +246,7 @@ def draw_workload(dims: Dims, seed: int = 0, threads: int | None = None):
         layers = [{n: f.result() for n, f in zip(LAYER_TENSORS, fl)} for fl in futs]
         pk = [p.result()[0] for p in pfx]
         pv = [p.result()[1] for p in pfx]
+    if variant.extras:
+        for l, w in enumerate(layers):
+            w.update(draw_extras(dims, l, seed))
     return layers, pk, pv, draw_hidden(dims, seed)

@@ -14,9 +14,20 @@ pytestmark = pytest.mark.skipif(not os.path.exists(pds.LIB_PATH),
 
 def _dims(**kw):
     base = dict(n_layers=2, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn_dim=768,
-                rope_theta=1.0e4, rms_eps=1e-5)
+                rope_theta=1.0e4, rms_eps=1e-5, rope_layout=0, rot_dim=0, freq_factors=None,
+                rope_mscale=0.0, attn_softcap=0.0, window=0)
     base.update(kw)
-    return pds.pds_dims(*[base[f] for f, _ in pds.pds_dims._fields_])
+    ff = base.pop("freq_factors")
+    d = pds.pds_dims(*[base[f] for f, _ in pds.pds_dims._fields_ if f != "freq_factors"][:8])
+    for f, _ in pds.pds_dims._fields_[8:]:
+        if f == "freq_factors":
+            if ff is not None:
+                arr = (ctypes.c_float * len(ff))(*ff)
+                d.freq_factors = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+                d._keep = arr
+        else:
+            setattr(d, f, base[f])
+    return d
 
 
 def _create(**kw):
@@ -42,6 +53,8 @@ def test_plan_create_accepts_the_served_shapes():
         assert st == pds.PDS_OK, pds.last_error()
         assert pds.pds_workspace_bytes(plan, 512) > 0
         assert pds.pds_workspace_bytes(plan, 0) == 0
+        # room for chunked attention grows with the prefix
+        assert (pds.pds_workspace_bytes(plan, 512, 32768) > pds.pds_workspace_bytes(plan, 512, 0))
         pds.pds_plan_destroy(plan)
 
 
@@ -66,7 +79,8 @@ def test_null_arguments():
     lib = pds.load()
     assert lib.pds_plan_create(None, None) == pds.PDS_EINVAL
     lib.pds_plan_destroy(None)
-    assert lib.pds_workspace_bytes(None, 8) == 0
+    assert lib.pds_workspace_bytes(None, 8, 0) == 0
+    assert lib.pds_workspace_bytes(None, 8, -1) == 0
     assert lib.pds_prefill_dense_stack(None, None, None, None, 0, 0, 1, None, None, None, 0,
                                        None) == pds.PDS_EINVAL
 
@@ -121,9 +135,12 @@ def test_component_entry_points_validate_on_host():
     assert lib.pds_gemm_bf16(0x100, 0x100, 0x100, 8, 192, 64, 0x100, 1 << 30, None) == pds.PDS_DECLINED
     assert lib.pds_gemm_bf16(0x100, 0x100, 0x100, 8, 256, 64, 0x100, 16, None) == pds.PDS_EINVAL
     assert pds.pds_gemm_workspace_bytes(512, 5120) >= pds.pds_gemm_workspace_bytes(8, 128) > 0
-    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 4, 0, 4, 2, 96, None) == pds.PDS_DECLINED
-    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 4, 0, 5, 2, 64, None) == pds.PDS_DECLINED
-    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 0, 0, 4, 2, 64, None) == pds.PDS_EINVAL
+    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 4, 0, 4, 2, 96, 0.0, 0, None, 0, None) == \
+        pds.PDS_DECLINED
+    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 4, 0, 5, 2, 64, 0.0, 0, None, 0, None) == \
+        pds.PDS_DECLINED
+    assert lib.pds_attention(0x100, 0x100, 0x100, 0x100, 0, 0, 4, 2, 64, 0.0, 0, None, 0, None) == \
+        pds.PDS_EINVAL
 
 
 def test_stack_marshals_pointer_arrays_once():
@@ -150,3 +167,67 @@ def test_stack_marshals_pointer_arrays_once():
         assert pds._layer_array(st._layers_c) is st._layers_c
     finally:
         st.close()
+
+
+@pytest.mark.parametrize("kw", [dict(rope_layout=1), dict(rot_dim=32), dict(rot_dim=64),
+                                dict(rope_layout=1, rot_dim=16),
+                                dict(freq_factors=[1.0 + i for i in range(32)]),
+                                dict(rope_mscale=1.2, attn_softcap=30.0, window=128)])
+def test_plan_create_accepts_the_served_variants(kw):
+    st, plan = _create(**kw)
+    assert st == pds.PDS_OK, pds.last_error()
+    pds.pds_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("kw", [dict(rot_dim=16), dict(rot_dim=48), dict(rope_layout=1, rot_dim=8)])
+def test_plan_create_declines_unserved_rotary_widths(kw):
+    st, plan = _create(**kw)
+    assert st == pds.PDS_DECLINED, pds.last_error()
+    assert not plan.value
+
+
+@pytest.mark.parametrize("kw", [dict(rope_layout=2), dict(rot_dim=-2), dict(rot_dim=66),
+                                dict(rot_dim=3), dict(rope_mscale=-1.0),
+                                dict(attn_softcap=-1.0), dict(attn_softcap=float("inf")),
+                                dict(window=-1), dict(freq_factors=[1.0] * 31 + [0.0]),
+                                dict(freq_factors=[1.0] * 31 + [float("nan")])])
+def test_plan_create_rejects_bad_variants(kw):
+    st, _ = _create(**kw)
+    assert st == pds.PDS_EINVAL, pds.last_error()
+
+
+def test_attention_entry_rejects_negative_options():
+    lib = pds.load()
+    args = (0x100, 0x100, 0x100, 0x100, 8, 0, 4, 2, 64)
+    assert lib.pds_attention(*args, -1.0, 0, None, 0, None) == pds.PDS_EINVAL
+    assert lib.pds_attention(*args, 0.0, -5, None, 0, None) == pds.PDS_EINVAL
+
+
+def test_plan_without_a_device_is_host_only():
+    """On a machine without a CUDA device the plan still validates and sizes
+    its workspace; a call then fails after admission instead of touching a GPU."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    st, plan = _create()
+    assert st == pds.PDS_OK
+    L = 2
+    layers = (pds.pds_layer * L)()
+    for l in range(L):
+        for f in pds.LAYER_FIELDS:
+            setattr(layers[l], f, 0x10000)
+    kc = (ctypes.c_void_p * L)(*([0x30000] * L))
+    vc = (ctypes.c_void_p * L)(*([0x40000] * L))
+    ws = pds.pds_workspace_bytes(plan, 8)
+    rc = pds.load().pds_prefill_dense_stack_device(plan, layers, kc, vc, 16, 0, 8, 0x50000,
+                                                   0x60000, 0x20000, ws, None)
+    assert rc == pds.PDS_ELAUNCH
+    assert "without a CUDA device" in pds.last_error()
+    pds.pds_plan_destroy(plan)
+
+
+def test_attention_workspace_sizes():
+    assert pds.pds_attention_workspace_bytes(512, 0, 24, 128) < \
+        pds.pds_attention_workspace_bytes(512, 32768, 24, 128)
+    assert pds.pds_attention_workspace_bytes(0, 0, 24, 128) == 0
+    assert pds.pds_attention_workspace_bytes(8, 0, 24, 96) == 0
