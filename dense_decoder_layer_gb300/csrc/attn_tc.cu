@@ -392,11 +392,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) tc_fence_after();
     };
+    // A warp whose 32 rows are all past the batch (a short last query tile,
+    // a decode step) keeps every barrier phase of the tile loop, one tile at a
+    // time, but computes nothing: the four warps of a lane group share their
+    // rows, so they are live or dead together.
+    const bool live = b0 + (sw_idx & 3) * 32 < a.B;
     for (int j = 0; j < n; ++j) {
       const int st = j & 1;
       wait(bar_s_full(st), (j >> 1) & 1);
       float sv[kPartKeys];
       float mx = -INFINITY;  // raw score maximum (the scale is positive)
+      if (ok && !live) {
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar_s_free(st));
+          mbar_arrive(bar_p_full);
+        }
+        // stay in step with the live warps: P_j's barrier phase completes only
+        // with their arrivals, so this warp's arrivals for tile j + 1 cannot
+        // count toward tile j's phases once O += P_j V_j has completed
+        wait(bar_pv, j & 1);
+        continue;
+      }
       if (ok) {
 #pragma unroll
         for (int c = 0; c < kPartKeys / 32; ++c) {
@@ -490,13 +507,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     // the row sum of all parts (in part order), while the last P.V runs;
     // then O row / l
-    named_bar_sync(1 + (warp & 3), 32 * kRowSplit);
-    xch[part * 128 + r] = l;
-    named_bar_sync(1 + (warp & 3), 32 * kRowSplit);
-    l = 0.f;
+    if (live) {
+      named_bar_sync(1 + (warp & 3), 32 * kRowSplit);
+      xch[part * 128 + r] = l;
+      named_bar_sync(1 + (warp & 3), 32 * kRowSplit);
+      l = 0.f;
 #pragma unroll
-    for (int q = 0; q < kRowSplit; ++q) l += xch[q * 128 + r];
-    wait(bar_pv, (n - 1) & 1);
+      for (int q = 0; q < kRowSplit; ++q) l += xch[q * 128 + r];
+      wait(bar_pv, (n - 1) & 1);
+    }
     // split: the second CTA's O part (float32, 16-byte chunks swizzled by the
     // row) goes to the first CTA at the K stages' offset, its row sum and
     // row maximum at the P buffer's offset
@@ -508,7 +527,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float* lmsg = reinterpret_cast<float*>(smem + C::kP0);  // [128] row sums, then [128] maxima
     if (chunked) {
       // this chunk's unnormalised O row part and the row's (reference max, sum)
-      if (ok) {
+      if (ok && live) {
         float* dst = a.o_part + (static_cast<size_t>(blockIdx.y) * kRows + r) * HD + part * kPartCols;
 #pragma unroll
         for (int c = 0; c < kPartCols / 16; ++c) {
@@ -523,7 +542,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                               make_float2(m_ref, l));
       }
     } else if (split && half == 1) {
-      if (ok) {
+      if (ok && live) {
 #pragma unroll
         for (int c = 0; c < kPartCols / 16; ++c) {
           float t[16];
@@ -558,7 +577,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive_cluster(mapa_shared(bar_m_ready, 1));  // O, P and K are done with here
       }
       wait(bar_m_recv, 0);
-      if (ok) {
+      if (ok && live) {
         // a row sees its own key, in one half or the other: m is finite (a
         // half that sees none of the row's keys has maximum -inf, weight 0)
         const float m1 = lmsg[128 + r];
@@ -591,7 +610,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
       }
-    } else if (ok) {
+    } else if (ok && live) {
       const float inv = 1.f / l;
       const int b = b0 + r;
       uint16_t* dst = a.o + (static_cast<size_t>(b) * a.H + h) * HD + part * kPartCols;

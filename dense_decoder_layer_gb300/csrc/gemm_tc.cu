@@ -182,14 +182,16 @@ struct SegIter {
   }
 };
 
-template <int BN>
+// Weight block and first row of piece h of column tile nt: the 128-row
+// boxes of a tile (BN / 128 of them), or for a CTA pair its half (BN / 2 rows).
+template <int BN, bool PAIR>
 __device__ __forceinline__ void b_source(const GemmArgs& g, int nt, int h, int& mi, int& row) {
   if (g.pair_mode) {
     mi = h;
     row = nt * 128;
     return;
   }
-  const int n0 = nt * BN + h * 128;
+  const int n0 = nt * BN + h * (PAIR ? BN / 2 : 128);
   if (n0 < g.wrows0) {
     mi = 0;
     row = n0;
@@ -483,6 +485,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
   const int m = mt * BM + row;
   const int m0w = mt * BM + (row & ~31);            // first row of this warp's 32
   const int rows = max(0, min(32, g.M - m0w));      // of which exist
+  if (rows == 0) return;                            // none: nothing to compute or store
   if constexpr (EPI == kEpiPlain || EPI == kEpiResid) {
     const int q = lane & 7;
     // the residual stream and the next GEMM's operand are read again within
@@ -676,9 +679,12 @@ __device__ __forceinline__ uint32_t epi_box(uint32_t sbase, int n_it, int b) {
 // this thread's epilogue reads, the contributors' accumulators are summed
 // in k order from zero (its own TMEM value in its place) and written back.
 // Two contributors' partial rows are in flight at once.
+// Rows past M hold zeros in every contributor (their A rows are zero-filled),
+// so their partials are neither stored nor read (row_ok false).
 template <int BN, int EPI>
 __device__ __forceinline__ void fixup_reduce_regs(const GemmArgs& g, const Fixup& fx,
-                                                  uint32_t taddr, int nt, int row, int ch) {
+                                                  uint32_t taddr, int nt, int row, int ch,
+                                                  bool row_ok) {
   using namespace sm100;
   constexpr int kOwned = owned_chunks<BN, EPI>();
 #pragma unroll 1
@@ -694,7 +700,7 @@ __device__ __forceinline__ void fixup_reduce_regs(const GemmArgs& g, const Fixup
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int c = c0 + u;
-        if (c <= fx.gl && c != fx.me) {
+        if (c <= fx.gl && c != fx.me && row_ok) {
           const float4* p = partial_slot(g, c, fx.r, fx.unit, BN) + static_cast<size_t>(j * 8) * BM + row;
 #pragma unroll
           for (int q = 0; q < 8; ++q) b[u][q] = __ldcg(p + q * BM);
@@ -709,7 +715,7 @@ __device__ __forceinline__ void fixup_reduce_regs(const GemmArgs& g, const Fixup
           tmem_load32(taddr + j * 32, own);
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] += own[q];
-        } else {
+        } else if (row_ok) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             v[4 * q] += b[u][q].x;
@@ -724,6 +730,132 @@ __device__ __forceinline__ void fixup_reduce_regs(const GemmArgs& g, const Fixup
   }
 }
 
+// Split tiles with at most this many rows (decode batches) are finished by
+// fixup_reduce_small.
+constexpr int kSmallRows = 8;
+
+// Finishes a split tile of at most kSmallRows rows with every epilogue
+// thread, in TMEM.  When all contributors' partial rows fit the epilogue
+// staging area (`stage`, 32 KB): every thread copies a few of them there
+// (all of its loads in flight at once), then every position is summed in k
+// order by one thread (this CTA's own partial, stored to its slot like the
+// others', in its place) and the rows' owning threads write the sums to
+// TMEM.  Otherwise each
+// position is summed by one thread, two contributors' loads at a time, and
+// the sums reach the owning threads through the staging area.  Called by
+// all epilogue threads (et = index).
+template <int BN, int EPI>
+__device__ __forceinline__ void fixup_reduce_small(const GemmArgs& g, const Fixup& fx,
+                                                   uint32_t taddr, int mt, int nt, int row,
+                                                   int ch, int et, float4* stage) {
+  using namespace sm100;
+  const int rv = min(BM, g.M - mt * BM);  // rows of the tile that exist (<= kSmallRows)
+  const int per = rv * (BN / 4);          // float4 of one contributor's rows
+  const int nc = fx.gl - fx.gf + 1;
+  const bool row_ok = row < rv;
+  constexpr int kOwned = owned_chunks<BN, EPI>();
+  constexpr int kStageF4 = 8 * 32 * 128 / 16;  // float4 in the staging area
+  if (nc * per <= kStageF4) {
+    const int items = nc * per;
+#pragma unroll 1
+    for (int b = et; b < items; b += 4 * kEpiThreads) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = b + u * kEpiThreads;
+        if (it < items) {
+          const int t = it / per, rem = it - t * per;
+          const int c4 = rem / rv, rr = rem - c4 * rv;
+          v[u] = __ldcg(partial_slot(g, fx.gf + t, fx.r, fx.unit, BN) + static_cast<size_t>(c4) * BM + rr);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (b + u * kEpiThreads < items) stage[b + u * kEpiThreads] = v[u];
+    }
+    named_bar_sync(1, kEpiThreads);
+    // each position summed in k order by one thread, into contributor 0's place
+    for (int pos = et; pos < per; pos += kEpiThreads) {
+      float4 acc = stage[pos];
+#pragma unroll 1
+      for (int t = 1; t < nc; ++t) {
+        const float4 x = stage[t * per + pos];
+        acc.x += x.x;
+        acc.y += x.y;
+        acc.z += x.z;
+        acc.w += x.w;
+      }
+      stage[pos] = acc;
+    }
+    named_bar_sync(1, kEpiThreads);
+#pragma unroll 1
+    for (int i = 0; i < kOwned; ++i) {
+      const int j = owned_chunk<BN, EPI>(ch, i);
+      if (!chunk_exists<BN, EPI>(g, nt, j)) continue;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 x = row_ok ? stage[(j * 8 + h * 4 + q) * rv + row]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[4 * q] = x.x;
+          v[4 * q + 1] = x.y;
+          v[4 * q + 2] = x.z;
+          v[4 * q + 3] = x.w;
+        }
+        tmem_store16(taddr + j * 32 + h * 16, v);
+      }
+    }
+    named_bar_sync(1, kEpiThreads);  // the staging area is free again
+    return;
+  }
+  float4* sums = stage;  // [BN/4][kSmallRows]
+  const int npos = per;
+  for (int p = et; p < npos; p += kEpiThreads) {
+    const int rr = p % rv, c4 = p / rv;  // row, float4 column (j * 8 + q)
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int c0 = fx.gf; c0 <= fx.gl; c0 += 2) {
+      float4 v[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        if (c0 + u <= fx.gl)
+          v[u] = __ldcg(partial_slot(g, c0 + u, fx.r, fx.unit, BN) + static_cast<size_t>(c4) * BM + rr);
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        if (c0 + u <= fx.gl) {
+          acc.x += v[u].x;
+          acc.y += v[u].y;
+          acc.z += v[u].z;
+          acc.w += v[u].w;
+        }
+    }
+    sums[c4 * kSmallRows + rr] = acc;
+  }
+  named_bar_sync(1, kEpiThreads);
+#pragma unroll 1
+  for (int i = 0; i < kOwned; ++i) {
+    const int j = owned_chunk<BN, EPI>(ch, i);
+    if (!chunk_exists<BN, EPI>(g, nt, j)) continue;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      float v[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 x = row_ok ? sums[(j * 8 + h * 4 + q) * kSmallRows + row]
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[4 * q] = x.x;
+        v[4 * q + 1] = x.y;
+        v[4 * q + 2] = x.z;
+        v[4 * q + 3] = x.w;
+      }
+      tmem_store16(taddr + j * 32 + h * 16, v);
+    }
+  }
+  named_bar_sync(1, kEpiThreads);  // the staging area is free again
+}
+
 // Finishes a split tile that this CTA completes as its last tile, in TMEM:
 // for each 32-column chunk this thread's epilogue reads, the contributors'
 // accumulators are summed in k order from zero (its own TMEM value in its
@@ -735,7 +867,7 @@ template <int BN, int EPI, bool PAIR>
 __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup& fx,
                                                   uint32_t taddr, int nt, int row, int ch,
                                                   uint8_t* sm, uint32_t sbase, int n_it,
-                                                  int box0) {
+                                                  int box0, bool row_ok) {
   using namespace sm100;
   constexpr int kOwned = owned_chunks<BN, EPI>();
   const int nother = fx.gl - fx.gf;  // contributors other than this CTA's group
@@ -748,11 +880,13 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
                          static_cast<uint32_t>(row) * 16u;
     const float4* src = partial_slot(g, contributor(t), fx.r, fx.unit, BN) +
                         static_cast<size_t>(j * 8) * BM + row;
+    if (row_ok) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + q * BM * 16u),
-                   "l"(src + q * BM)
-                   : "memory");
+      for (int q = 0; q < 8; ++q)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + q * BM * 16u),
+                     "l"(src + q * BM)
+                     : "memory");
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
   const int nloads = kOwned * nother;
@@ -787,13 +921,15 @@ __device__ __forceinline__ void fixup_reduce_smem(const GemmArgs& g, const Fixup
       }
       const uint32_t pb = epi_box<BN, PAIR>(sbase, n_it, box0 + ch * 2 + (k & 1)) +
                           static_cast<uint32_t>(row) * 16u;
+      if (row_ok) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 p = *sm_at<float4>(sm, sbase, pb + q * BM * 16u);
-        v[4 * q] += p.x;
-        v[4 * q + 1] += p.y;
-        v[4 * q + 2] += p.z;
-        v[4 * q + 3] += p.w;
+        for (int q = 0; q < 8; ++q) {
+          const float4 p = *sm_at<float4>(sm, sbase, pb + q * BM * 16u);
+          v[4 * q] += p.x;
+          v[4 * q + 1] += p.y;
+          v[4 * q + 2] += p.z;
+          v[4 * q + 3] += p.w;
+        }
       }
       ++k;
     }
@@ -827,6 +963,7 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
   const int m = mt * BM + row;
   const int m0w = mt * BM + lane_grp * 32;
   const bool warp_live = m0w < g.M;
+  if (!warp_live) return true;  // no row of this warp exists: nothing to compute or store
   const uint64_t pol_keep = policy_evict_last();
   const uint32_t sw = static_cast<uint32_t>(row & 7);
   const uint32_t a_stage = smem_u32(st.base);  // this warp's 32 rows x 64 bf16 of the operand
@@ -1153,14 +1290,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (PAIR) {
           // this CTA's half of the pair's BN weight rows
           int mi, row;
-          b_source<BN>(g, nt, static_cast<int>(prank), mi, row);
+          b_source<BN, true>(g, nt, static_cast<int>(prank), mi, row);
           tma_load_2d_pair(sbase + s * C::kStage + C::kABytes, &maps.b[mi], full_bar(s), kb * BK,
                            row, pol_w);
         } else {
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h) {
             int mi, row;
-            b_source<BN>(g, nt, h, mi, row);
+            b_source<BN, false>(g, nt, h, mi, row);
             tma_load_2d(sbase + s * C::kStage + C::kABytes + h * 16384u, &maps.b[mi], bar_full(s),
                         kb * BK, row, pol_w);
           }
@@ -1318,7 +1455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mt * BM + row < g.M) rscale = row_scale(g.swiglu.rs, mt * BM + row);
       } else if constexpr (EPI == kEpiQkv) {
         if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
-        rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
+        // (a small tile loads the table after its reduction: see below)
+        if (PAIR || g.M - mt * BM > kSmallRows) rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
       } else if constexpr (EPI == kEpiQkvX) {
         if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
       } else if constexpr (EPI == kEpiResid) {
@@ -1334,7 +1472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = mt + nt * g.tiles_m;
       Fixup fx{false, 0, 0, grp, rank, unit};
       bool run = true;
-      if constexpr (EPI == kEpiResid && PAIR) {
+      if constexpr (EPI == kEpiResid && PAIR && BN == 256) {
         if (g.split > 1) {
           // the CTA's only tile, finished with the cluster's other pairs
           const bool ok = split_resid_epilogue<BN>(
@@ -1359,10 +1497,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!chunk_exists<BN, EPI>(g, nt, j)) continue;
           float v[32];
           tmem_load32(taddr + j * 32, v);
+          if (mt * BM + row < g.M) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            __stcg(mine + (j * 8 + q) * BM + row,
-                   make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+            for (int q = 0; q < 8; ++q)
+              __stcg(mine + (j * 8 + q) * BM + row,
+                     make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+          }
         }
         __threadfence();
         named_bar_sync(1, kEpiThreads);
@@ -1384,14 +1524,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // partials added in k order), then the epilogue reads TMEM as for an
         // unsplit tile.  The CTA's last tile stages the partials in the
         // drained stages (after the residual boxes of a residual GEMM).
-        if (split) {
+        // (a pair tile has two full row tiles: never a small one)
+        if (!PAIR && split && g.M - mt * BM <= kSmallRows) {
+          if constexpr (!PAIR)
+            fixup_reduce_small<BN, EPI>(g, fx, taddr, mt, nt, row, ch,
+                                        static_cast<int>(threadIdx.x) - kEpiFirstThread,
+                                        reinterpret_cast<float4*>(smem + S * C::kStage + C::kMiscBytes));
+        } else if (split) {
+          const bool row_ok = mt * BM + row < g.M;
           if (last) {
             fixup_reduce_smem<BN, EPI, PAIR>(g, fx, taddr, nt, row, ch, smem, sbase, it1 - it0,
-                                             EPI == kEpiResid ? C::kResBoxes : 0);
+                                             EPI == kEpiResid ? C::kResBoxes : 0, row_ok);
           } else {
-            fixup_reduce_regs<BN, EPI>(g, fx, taddr, nt, row, ch);
+            fixup_reduce_regs<BN, EPI>(g, fx, taddr, nt, row, ch, row_ok);
           }
           fx.active = false;
+        }
+        if constexpr (EPI == kEpiQkv && !PAIR) {
+          if (g.M - mt * BM <= kSmallRows) rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
         }
         if (EPI == kEpiResid && last) {
           auto acc = [&](int j, float (&v)[32]) { tmem_load32(taddr + j * 32, v); };
@@ -1585,6 +1735,15 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   }
   const int ctas = std::min({c.num_sms > 0 ? c.num_sms : 148, kGemmMaxGrid, max_grid});
   const int gmax = std::max(1, std::min(ctas / gs, g.total / kMinItersPerCta));
+  if (g.tiles_m == 1 && M <= kSmallRows) {
+    // A decode batch: the split tiles' partials are a few rows, reduced by
+    // all epilogue threads at once (fixup_reduce_small), so every column tile
+    // gets as many CTAs as fill the GPU, each an equal k range.
+    const int c = std::max(1, std::min(ctas / g.tiles_n, g.kb / kMinItersPerCta));
+    g.groups = g.tiles_n * c;
+    g.grid = g.groups * gs;
+    return;
+  }
   if (g.tiles_m == 1) {
     // A single row tile streams every weight byte once and is bound by how
     // fast the CTAs pull weights in, which wants many CTAs; but each extra
@@ -1787,8 +1946,11 @@ pds_status tc_gemm_plain(TcContext& c, const uint16_t* A, const uint16_t* W, flo
 
 pds_status tc_gemm_resid(TcContext& c, const uint16_t* A, const uint16_t* W, int M, int N, int K,
                          const ResidEpilogue& e, cudaStream_t st, std::string* err) {
-  // a single row tile: 128-wide tiles (twice the tiles to spread the
-  // weights over; measured faster for both residual GEMMs at M = 128)
+  // A single row tile: 128-wide tiles (twice the tiles to spread the
+  // weights over; measured faster for both residual GEMMs at M = 128).
+  // Pairs of row tiles: 256 x 256 pair tiles (256 x 128 pair tiles without
+  // a k split were measured slower at M = 512: a 256 x 128 x 64 pair step
+  // took as long as a 256 x 256 x 64 one).
   const int bn = (N % 256 == 0 && M > BM) ? 256 : 128;
   GemmArgs g{};
   g.wrows0 = N;
