@@ -647,16 +647,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // Combines the chunks of the chunked mode: for each query tile, row and
 // head, O = sum_c O_c 2^(m_c - m) / sum_c l_c 2^(m_c - m), m = max_c m_c, in
-// chunk order.  One warp per (query tile, head, row); lane i holds columns
-// 4i .. 4i + 3.
+// chunk order.  One warp per (query tile, head, row) -- rows of a tile up to
+// the batch (merge_rows) -- lane i holds columns 4i .. 4i + 3.
+__host__ __device__ __forceinline__ int merge_rows(int B) { return B < kRows ? B : kRows; }
 template <int HD>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnArgs a) {
   sm100::grid_dep_wait();
   sm100::grid_dep_launch();
   const int warp = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nq = (a.B + kRows - 1) / kRows;
-  const int r = warp % kRows;
-  int rest = warp / kRows;
+  const int rpt = merge_rows(a.B);
+  const int r = warp % rpt;
+  int rest = warp / rpt;
   const int h = rest % a.H;
   const int tq = rest / a.H;  // 0: the last query tile (units are ordered that way)
   if (tq >= nq) return;
@@ -791,7 +793,7 @@ pds_status launch_attn_tc(TcContext& c, const uint16_t* q, const uint16_t* k, co
     cudaError_t ce = cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, VAR>, maps, args);
     if (ce == cudaSuccess) {
       cudaLaunchConfig_t mc = {};
-      mc.gridDim = dim3((tiles * kRows + 7) / 8);
+      mc.gridDim = dim3((tiles * merge_rows(B) + 7) / 8);
       mc.blockDim = dim3(256);
       mc.stream = st;
       mc.attrs = at;

@@ -804,9 +804,10 @@ __device__ __forceinline__ void fixup_reduce_small(const GemmArgs& g, const Fixu
           v[4 * q + 2] = x.z;
           v[4 * q + 3] = x.w;
         }
-        tmem_store16(taddr + j * 32 + h * 16, v);
+        tmem_store16_nowait(taddr + j * 32 + h * 16, v);
       }
     }
+    tmem_wait_st();
     named_bar_sync(1, kEpiThreads);  // the staging area is free again
     return;
   }
@@ -850,9 +851,10 @@ __device__ __forceinline__ void fixup_reduce_small(const GemmArgs& g, const Fixu
         v[4 * q + 2] = x.z;
         v[4 * q + 3] = x.w;
       }
-      tmem_store16(taddr + j * 32 + h * 16, v);
+      tmem_store16_nowait(taddr + j * 32 + h * 16, v);
     }
   }
+  tmem_wait_st();
   named_bar_sync(1, kEpiThreads);  // the staging area is free again
 }
 
@@ -1738,8 +1740,16 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   if (g.tiles_m == 1 && M <= kSmallRows) {
     // A decode batch: the split tiles' partials are a few rows, reduced by
     // all epilogue threads at once (fixup_reduce_small), so every column tile
-    // gets as many CTAs as fill the GPU, each an equal k range.
-    const int c = std::max(1, std::min(ctas / g.tiles_n, g.kb / kMinItersPerCta));
+    // gets as many CTAs as fill the GPU, each an equal k range -- an aligned
+    // one (c dividing the k-blocks, every CTA on one tile) unless that costs
+    // more than a quarter of the CTAs.
+    const int c_max = std::max(1, std::min(ctas / g.tiles_n, g.kb / kMinItersPerCta));
+    int c = c_max;
+    for (int d = c_max; d >= 1; --d)
+      if (g.kb % d == 0) {
+        if (4 * d >= 3 * c_max) c = d;
+        break;
+      }
     g.groups = g.tiles_n * c;
     g.grid = g.groups * gs;
     return;

@@ -352,6 +352,35 @@ __device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32
       : "memory");
 }
 
+// 16 consecutive columns of this thread's lane from registers, without
+// waiting (tmem_wait_st makes them visible to this thread's later loads).
+__device__ __forceinline__ void tmem_store16_nowait(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Atomic add at GPU scope with acquire-release semantics: after a CTA
+// barrier, one thread's call publishes the CTA's earlier writes and, with a
+// barrier after it, makes other CTAs' writes published the same way visible
+// to the whole CTA.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // 16 consecutive columns of this thread's lane from registers; waits until
 // the stores are done.
 __device__ __forceinline__ void tmem_store16(uint32_t taddr, const float (&v)[16]) {
