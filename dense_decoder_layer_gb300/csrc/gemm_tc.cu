@@ -38,6 +38,15 @@
 // exchange column slices of their accumulators through distributed shared
 // memory and each finishes its own slice (see split_resid_epilogue).
 //
+// Row-split cluster (a single row tile of 9..128 rows, any epilogue): a
+// cluster of c CTAs (3 to 8) computes one 128 x BN tile, CTA q over the
+// q-th of c k ranges; the CTAs exchange row slices of their accumulators
+// through distributed shared memory and CTA q finishes rows [q R, q R + R),
+// R = 128 / c rounded up to a multiple of 8 (see rsplit_exchange).  Every
+// weight byte is read by one CTA, and the weights of a GEMM come in over up
+// to eight times as many SMs as it has column tiles, with no partial tile
+// in global memory and no CTA reducing the others' partials alone.
+//
 // Epilogues (the stack's fusions; frink-models 0.29.0
 // src/decoder/cuda_prefill.rs, module doc: everything between the seven
 // matmuls of a layer is a kernel):
@@ -113,6 +122,11 @@ struct GemmArgs {
   // CTAs computes one 256 x BN tile, pair q over the q-th of `split` equal
   // k ranges, and finishes it through distributed shared memory.  0: off.
   int split;
+  // Row-split cluster (a single row tile of more than kSmallRows rows): each
+  // cluster of `rsplit` CTAs computes one 128 x BN tile, CTA q over the q-th
+  // of rsplit k ranges, and CTA q finishes its slice of rows (see
+  // rsplit_exchange).  0: off.
+  int rsplit;
   int wrows0, wrows1;  // rows of weight blocks 0 and 1 (concatenated along N)
   int pair_mode;       // W tile = 128 rows of block 0 then the same rows of block 1
   uint32_t* status;
@@ -153,6 +167,7 @@ struct Cfg {
   static constexpr uint32_t kStageBytes = 8 * 32 * 128;         // epilogue staging, 4 KB a warp
   static constexpr size_t kSmem = 1024 + kStages * kStage + kMiscBytes + kStageBytes;
   static_assert(kBars * 8 + 16 <= 1024, "barrier area");
+
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
@@ -275,17 +290,23 @@ __device__ __forceinline__ void stage_bf16(const Stage& st, int lane, int c, con
                                      __uint_as_float(pack_bf16x2(v[8 * q + 6], v[8 * q + 7])));
 }
 
+// The rows of a warp's 32 that an epilogue stores: lo <= r < hi.
+struct Rows {
+  int lo, hi;
+  __device__ __forceinline__ bool has(int r) const { return r >= lo && r < hi; }
+};
+
 // Store staged bf16 chunks c..c+3 (32 columns, 64 bytes) of the warp's rows
-// r < rows to dst_row0 + r * ld, eight rows per instruction.
+// in `rows` to dst_row0 + r * ld, eight rows per instruction.
 __device__ __forceinline__ void flush_bf16(const Stage& st, int c, uint16_t* dst_row0, size_t ld,
-                                           int rows, int lane) {
+                                           Rows rows, int lane) {
   // activations are read again soon: keep them in L2 while weights stream by
   const uint64_t pol = sm100::policy_evict_last();
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = i * 8 + (lane >> 2), q = lane & 3;
-    if (r < rows)
+    if (rows.has(r))
       sm100::st_global_hint(reinterpret_cast<float4*>(dst_row0 + r * ld + q * 8), st.at(r, c + q),
                             pol);
   }
@@ -371,11 +392,10 @@ __device__ __forceinline__ void ld_f32x16(const float* p, float (&v)[16]) {
 template <int BN>
 __device__ __forceinline__ void qkv_general_epilogue(const GemmArgs& g, uint32_t taddr, int mt,
                                                      int nt, int row, int ch, int lane, float r,
-                                                     const Stage& st) {
+                                                     const Stage& st, Rows rows) {
   const QkvEpilogue& e = g.qkv;
   const int m = mt * BM + row;
   const int m0w = mt * BM + (row & ~31);
-  const int rows = max(0, min(32, g.M - m0w));
   const int c0 = nt * BN + ch * 128;  // first of this thread's 128 columns of [q | k | v]
   if (c0 >= e.q_width + 2 * e.kv_width) return;
   const int blk = c0 < e.q_width ? 0 : (c0 < e.q_width + e.kv_width ? 1 : 2);
@@ -477,15 +497,16 @@ __device__ __forceinline__ void qkv_general_epilogue(const GemmArgs& g, uint32_t
 }
 
 // The fused epilogue of one tile for this thread (row `row` of the tile,
-// column half `ch`); r is the row's RMSNorm scale (SwiGLU and QKV).
+// column half `ch`); r is the row's RMSNorm scale (SwiGLU and QKV).  The
+// warp stores its rows r (of its 32) with wlo <= r < whi that exist.
 template <int BN, int EPI>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, int mt, int nt,
                                              int row, int ch, int lane, float r, const Stage& st,
-                                             RopeRegs& rr) {
+                                             RopeRegs& rr, int wlo = 0, int whi = 32) {
   const int m = mt * BM + row;
-  const int m0w = mt * BM + (row & ~31);            // first row of this warp's 32
-  const int rows = max(0, min(32, g.M - m0w));      // of which exist
-  if (rows == 0) return;                            // none: nothing to compute or store
+  const int m0w = mt * BM + (row & ~31);                   // first row of this warp's 32
+  const Rows rows{wlo, min(whi, g.M - m0w)};               // of which it stores
+  if (rows.hi <= rows.lo) return;                          // none: nothing to compute or store
   if constexpr (EPI == kEpiPlain || EPI == kEpiResid) {
     const int q = lane & 7;
     // the residual stream and the next GEMM's operand are read again within
@@ -505,7 +526,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int rr = i * 4 + (lane >> 3);
-          r4[i] = rr < rows ? *reinterpret_cast<const float4*>(
+          r4[i] = rows.has(rr) ? *reinterpret_cast<const float4*>(
                                   e.resid + static_cast<size_t>(m0w + rr) * g.resid_n + n0 + 4 * q)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -523,15 +544,15 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
         const int rr = i * 4 + (lane >> 3);
         const float4 a4 = st.at(rr, q);
         if constexpr (EPI == kEpiPlain) {
-          if (rr < rows)
+          if (rows.has(rr))
             *reinterpret_cast<float4*>(g.c_out + static_cast<size_t>(m0w + rr) * g.ldc + n0 + 4 * q) = a4;
         } else {
           const ResidEpilogue& e = g.resid;
           const float4 h4 = make_float4(r4[i].x + a4.x, r4[i].y + a4.y, r4[i].z + a4.z, r4[i].w + a4.w);
           const size_t off = static_cast<size_t>(m0w + rr) * g.resid_n + n0 + 4 * q;
-          if (rr < rows) sm100::st_global_hint(reinterpret_cast<float4*>(e.out + off), h4, pol_keep);
+          if (rows.has(rr)) sm100::st_global_hint(reinterpret_cast<float4*>(e.out + off), h4, pol_keep);
           if (e.gain) {
-            if (rr < rows)
+            if (rows.has(rr))
               sm100::st_global_hint(
                   reinterpret_cast<uint2*>(e.a_out + off),
                   make_uint2(pack_bf16x2(h4.x * g4.x, h4.y * g4.y), pack_bf16x2(h4.z * g4.z, h4.w * g4.w)),
@@ -552,7 +573,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int rr = i * 4 + (lane >> 3);
-              if (rr < rows)
+              if (rows.has(rr))
                 e.ss_out[static_cast<size_t>(m0w + rr) * (g.resid_n / 64) + (n0 - 32) / 64] = ss[i];
             }
           }
@@ -580,7 +601,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& g, uint32_t taddr, 
     }
   } else if constexpr (EPI == kEpiQkvX) {
     static_assert(BN == 256, "the QKV tile holds whole heads in each 128-column half");
-    qkv_general_epilogue<BN>(g, taddr, mt, nt, row, ch, lane, r, st);
+    qkv_general_epilogue<BN>(g, taddr, mt, nt, row, ch, lane, r, st, rows);
   } else {
     static_assert(BN == 256, "the QKV tile holds whole heads in each 128-column half");
     const QkvEpilogue& e = g.qkv;
@@ -1037,6 +1058,132 @@ __device__ __forceinline__ bool resid_epilogue_smem(const GemmArgs& g, const Gem
   return true;
 }
 
+// Rows each CTA of a row-split cluster of c finishes: 128 / c rounded up to
+// a multiple of 8 (the last slices may be short or empty).
+__host__ __device__ __forceinline__ int rsplit_rows(int c) { return ((BM + c - 1) / c + 7) & ~7; }
+
+// Row-split cluster: CTA `me` of the cluster has computed the me-th k range
+// of the tile into TMEM and finishes rows [me R, me R + R).
+//  1. Once every other CTA of the cluster has said that its stages are free
+//     (its accumulator is complete), each warp writes each 32-column chunk
+//     of its rows into a shared-memory box of its own (32 rows x 128 bytes,
+//     16-byte pieces XOR-swizzled by row) and bulk-copies the rows of each
+//     other CTA's slice into that CTA's drained stages, laid out
+//     [contributor t][chunk][row of the slice][128 bytes].  The received
+//     slices and the outgoing boxes share the drained stages, none reused.
+//  2. Once its own slices have landed, the warps that hold the slice's rows
+//     in TMEM add the contributions in k order (cluster rank order, from
+//     zero, its own in its place), a 32-column chunk at a time with each
+//     contributor's 32 values loaded at once, and write the sums back to
+//     TMEM for the epilogue.
+// Returns false if a wait gave up.
+template <int BN, int EPI>
+__device__ __forceinline__ bool rsplit_exchange(const GemmArgs& g, uint32_t taddr, int row, int ch,
+                                                int lane, uint8_t* sm, uint32_t sbase,
+                                                uint32_t bar_ready, uint32_t bar_recv,
+                                                volatile int* abort_flag, int me, bool leader) {
+  using namespace sm100;
+  constexpr int kOwned = owned_chunks<BN, EPI>();
+  constexpr int kChunks = BN / 32;
+  const int c = g.rsplit, R = rsplit_rows(c);
+  const int lo = me * R, hs = lo + R, hi = min(g.M, hs);  // the rows this CTA finishes
+  auto recv_off = [&](int t, int j, int r) {
+    return static_cast<uint32_t>(((t * kChunks + j) * R + r) * 128);
+  };
+  const uint32_t recv_bytes = static_cast<uint32_t>((c - 1) * R * BN * 4);
+  if (leader) {
+    mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>((c - 1) * max(0, hi - lo) * BN * 4));
+    for (int p = 0; p < c; ++p)
+      if (p != me) mbar_arrive_cluster(mapa_shared(bar_ready, static_cast<uint32_t>(p)));
+  }
+  if (!mbar_wait(bar_ready, 0, abort_flag, g.status)) return false;
+  tc_fence_after();
+  const int w0 = row & ~31, lg = w0 / 32;  // this warp's rows w0 .. w0 + 31
+  const uint32_t sw = static_cast<uint32_t>(row & 7);
+  {
+    // lane group l holds rows of other slices that exist
+    auto sends_of = [&](int l) {
+      return 32 * l < g.M && (32 * l < lo || min(32 * l + 32, g.M) > hs);
+    };
+    // this warp's boxes: a slot per lane group that sends, two halves each
+    int slot = 0;
+    for (int l = 0; l < lg; ++l) slot += sends_of(l) ? 1 : 0;
+    if (sends_of(lg)) {
+#pragma unroll 1
+      for (int k = 0; k < kOwned; ++k) {
+        const int j = owned_chunk<BN, EPI>(ch, k);
+        const uint32_t box =
+            sbase + recv_bytes + static_cast<uint32_t>(((slot * 2 + ch) * kOwned + k) * 4096);
+        float v[32];
+        tmem_load32(taddr + j * 32, v);
+        const uint32_t mine_row = box + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          *sm_at<float4>(sm, sbase, mine_row + ((static_cast<uint32_t>(q4) ^ sw) << 4)) =
+              make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // the existing rows of each other CTA's slice among this warp's
+          for (int p = w0 / R; p < c && p * R < w0 + 32; ++p) {
+            if (p == me) continue;
+            const int a = max(w0, p * R), b = min(min(w0 + 32, p * R + R), g.M);
+            if (a >= b) continue;
+            const int t = me < p ? me : me - 1;
+            bulk_copy_to_cluster(
+                mapa_shared(sbase + recv_off(t, j, a - p * R), static_cast<uint32_t>(p)),
+                box + static_cast<uint32_t>(a - w0) * 128u, static_cast<uint32_t>(b - a) * 128u,
+                mapa_shared(bar_recv, static_cast<uint32_t>(p)));
+          }
+        }
+      }
+    }
+  }
+  if (!mbar_wait(bar_recv, 0, abort_flag, g.status)) return false;
+  // TMEM accesses are warp-wide: a warp holding any finished row takes part
+  if (w0 >= hi || w0 + 32 <= lo) return true;
+  const bool mine = row >= lo && row < hi;
+  const int r = mine ? row - lo : 0;
+#pragma unroll 1
+  for (int i = 0; i < kOwned; ++i) {
+    const int j = owned_chunk<BN, EPI>(ch, i);
+    float own[32];
+    tmem_load32(taddr + j * 32, own);
+    if (mine) {
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = 0.f;
+#pragma unroll 1
+      for (int p = 0; p < c; ++p) {
+        if (p == me) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] += own[e];
+        } else {
+          // the contributor's 32 values, all eight loads in flight at once
+          const uint32_t base = sbase + recv_off(p < me ? p : p - 1, j, r);
+          float4 x[8];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            x[q4] = *sm_at<float4>(sm, sbase, base + ((static_cast<uint32_t>(q4) ^ sw) << 4));
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            v[4 * q4] += x[q4].x;
+            v[4 * q4 + 1] += x[q4].y;
+            v[4 * q4 + 2] += x[q4].z;
+            v[4 * q4 + 3] += x[q4].w;
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) own[e] = v[e];
+    }
+    tmem_store16_nowait(taddr + j * 32, reinterpret_cast<const float(&)[16]>(own[0]));
+    tmem_store16_nowait(taddr + j * 32 + 16, reinterpret_cast<const float(&)[16]>(own[16]));
+  }
+  tmem_wait_st();
+  return true;
+}
+
 // The gains of the BN columns of column tile nt into shared memory, by the
 // epilogue threads, before they wait for the CTA's last accumulator (the
 // gain is a weight: it does not wait for the previous kernel).
@@ -1180,9 +1327,12 @@ __device__ __forceinline__ bool split_resid_epilogue(
                                        mine.first, acc);
 }
 
-template <int BN, int EPI, bool PAIR>
+// RSPLIT: the row-split cluster schedule (g.rsplit > 1; non-pair only), a
+// separate instantiation so that neither schedule's registers burden the other.
+template <int BN, int EPI, bool PAIR, bool RSPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g) {
+  static_assert(!(PAIR && RSPLIT), "a row-split cluster computes single row tiles");
   using namespace sm100;
   using C = Cfg<BN, PAIR>;
   constexpr int S = C::kStages;
@@ -1221,7 +1371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_drain, 1);
     for (int f = 0; f < 4; ++f) mbar_init(bar_res0 + 8u * f, 1);
-    mbar_init(bar_ready, g.split > 1 ? g.split - 1 : 1);
+    mbar_init(bar_ready, g.split > 1 ? g.split - 1 : (RSPLIT ? g.rsplit - 1 : 1));
     mbar_init(bar_recv, 1);
     *abort_flag = 0;
     mbar_init_fence();
@@ -1282,10 +1432,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // A (activations) is re-read by every column tile: keep it.  A weight
       // box is read once when one cluster (or CTA) holds all the row tiles of
-      // its group: let it go first; otherwise the group's other CTAs read it
-      // again right away: normal priority.
+      // its group, or in a row-split cluster (one CTA per k range): let it
+      // go first; otherwise the group's other CTAs read it again right away:
+      // normal priority.
       const uint64_t pol_a = policy_evict_last();
-      const uint64_t pol_w = g.cs == g.gs ? policy_evict_first() : policy_evict_normal();
+      const uint64_t pol_w =
+          (g.cs == g.gs || RSPLIT) ? policy_evict_first() : policy_evict_normal();
       // where a stage's copies complete: the pair leader's barrier, or our own
       auto full_bar = [&](int s) { return PAIR ? mapa_shared(bar_full(s), lead) : bar_full(s); };
       auto load_w = [&](int s, int nt, int kb) {
@@ -1352,7 +1504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The last tile's residual, into the stages as the last MMAs free them
       // (continuing the ring as if they were further k-blocks).  A split
       // tile's residual is loaded too: this CTA may be the one to finish it.
-      if (EPI == kEpiResid && ok && it1 > it0) {
+      // (a row-split CTA's epilogue reads the residual rows it finishes itself)
+      if (EPI == kEpiResid && ok && it1 > it0 && !RSPLIT) {
         const uint64_t pol_r = policy_evict_first();  // the residual's last read
         // the whole tile's boxes, or the slice this CTA finishes in a split
         int rfirst = 0, rcount = C::kResBoxes;
@@ -1458,7 +1611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if constexpr (EPI == kEpiQkv) {
         if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
         // (a small tile loads the table after its reduction: see below)
-        if (PAIR || g.M - mt * BM > kSmallRows) rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
+        if (PAIR || (g.M - mt * BM > kSmallRows && !RSPLIT))
+          rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
       } else if constexpr (EPI == kEpiQkvX) {
         if (mt * BM + row < g.M) rscale = row_scale(g.qkv.rs, mt * BM + row);
       } else if constexpr (EPI == kEpiResid) {
@@ -1488,7 +1642,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
       }
-      if (!(k0 == 0 && k1 == g.kb)) {
+      // rows of the warp's 32 its epilogue stores
+      int wlo = 0, whi = 32;
+      bool gave_up = false;
+      if constexpr (!PAIR) {
+        if constexpr (RSPLIT) {
+          // the CTA's only tile: exchange rows with the cluster, then the
+          // epilogue of the rows this CTA finishes
+          const int me = static_cast<int>(crank), R = rsplit_rows(g.rsplit);
+          gave_up = !rsplit_exchange<BN, EPI>(g, taddr, row, ch, lane, smem, sbase, bar_ready,
+                                              bar_recv, abort_flag, me, leader);
+          wlo = max(0, me * R - lane_grp * 32);
+          whi = min(32, me * R + R - lane_grp * 32);
+          run = !gave_up && wlo < whi;
+          if constexpr (EPI == kEpiQkv) {
+            if (run) rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
+          }
+        }
+      }
+      if (!RSPLIT && !(k0 == 0 && k1 == g.kb)) {
         const int slot = (it0 / g.kb == unit) ? 0 : 1;
         float4* mine = reinterpret_cast<float4*>(g.partials) +
                        static_cast<size_t>(cta * 2 + slot) * (BM * BN / 4);
@@ -1545,7 +1717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (EPI == kEpiQkv && !PAIR) {
           if (g.M - mt * BM <= kSmallRows) rope_prefetch<BN>(g, nt, ch, mt * BM + row, rr);
         }
-        if (EPI == kEpiResid && last) {
+        if (EPI == kEpiResid && last && !RSPLIT) {
           auto acc = [&](int j, float (&v)[32]) { tmem_load32(taddr + j * 32, v); };
           if (!resid_epilogue_smem<BN, PAIR>(g, maps, mt, nt, row, ch, lane, smem, sbase, it1 - it0,
                                              bar_res0, abort_flag, st,
@@ -1553,7 +1725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ch * (BN / 64), BN / 64, 0, acc))
             break;
         } else {
-          run_epilogue<BN, EPI>(g, taddr, mt, nt, row, ch, lane, rscale, st, rr);
+          run_epilogue<BN, EPI>(g, taddr, mt, nt, row, ch, lane, rscale, st, rr, wlo, whi);
         }
         if (split && leader) g.counters[tile] = 0;
       }
@@ -1569,6 +1741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar_tempty(ab));
         }
       }
+      if (gave_up) break;
       ++sg;
     }
   } else {
@@ -1685,8 +1858,24 @@ pds_status get_map(TcContext& c, CUtensorMap* out, const void* p, uint64_t inner
   return PDS_OK;
 }
 
+// Shared memory a row-split CTA of a cluster of c needs in its drained
+// stages (the worst CTA of the cluster): the other CTAs' slices of its rows
+// and a box per 32-column chunk of each lane group it sends rows from.
+int rsplit_stage_bytes(int bn, int c) {
+  const int R = rsplit_rows(c);
+  int worst = 0;
+  for (int me = 0; me < c; ++me) {
+    const int lo = me * R, hs = std::min(BM, lo + R);
+    int slots = 0;
+    for (int l = 0; l < BM / 32; ++l) slots += (32 * l < lo || 32 * l + 32 > hs) ? 1 : 0;
+    worst = std::max(worst, (c - 1) * R * bn * 4 + slots * bn * 128);
+  }
+  return worst;
+}
+
 void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, int bn,
-                   int max_grid = kGemmMaxGrid, bool allow_pair = true, int split = 0) {
+                   int max_grid = kGemmMaxGrid, bool allow_pair = true, int split = 0,
+                   bool allow_rsplit = true) {
   g.M = M;
   g.K = K;
   g.tiles_m = (M + BM - 1) / BM;
@@ -1705,6 +1894,7 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   g.cs = 1;
   g.pair = 0;
   g.split = 0;
+  g.rsplit = 0;
   if (bn == 256 && gs % 2 == 0 && allow_pair && split != 0) {
     // Cluster split-K (residual epilogues only; split = 0 elsewhere): one
     // cluster of 2S CTAs per 256-row pair tile when the pair tiles alone
@@ -1754,6 +1944,29 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
     g.grid = g.groups * gs;
     return;
   }
+  if (g.tiles_m == 1 && allow_rsplit) {
+    // A single row tile of more rows streams every weight byte once and is
+    // bound by how fast its CTAs pull weights in (a CTA keeps its stages'
+    // bytes in flight, no more): it wants many CTAs on each tile, which the
+    // row-split cluster gives without a serial reduction -- each of the c
+    // CTAs of a tile's cluster takes 1/c of the k-blocks and finishes 1/c
+    // of the rows.  The largest c in 3..8 that leaves every CTA two
+    // k-blocks, keeps all clusters on the GPU at once and whose exchange
+    // fits the drained stages (c <= 4 for 256-wide tiles).  (Measured at
+    // M = 128 on GB300: a split in two lost to the unsplit schedule, whose
+    // CTAs are then one per column tile.)
+    const int stage_bytes = bn == 256 ? Cfg<256>::kStages * static_cast<int>(Cfg<256>::kStage)
+                                      : Cfg<128>::kStages * static_cast<int>(Cfg<128>::kStage);
+    for (int cc = 8; cc >= 3; --cc) {
+      if (2 * cc > g.kb || g.tiles_n * cc > ctas || rsplit_stage_bytes(bn, cc) > stage_bytes)
+        continue;
+      g.rsplit = cc;
+      g.cs = cc;
+      g.groups = g.tiles_n * cc;
+      g.grid = g.groups;
+      return;
+    }
+  }
   if (g.tiles_m == 1) {
     // A single row tile streams every weight byte once and is bound by how
     // fast the CTAs pull weights in, which wants many CTAs; but each extra
@@ -1799,11 +2012,11 @@ void make_schedule(GemmArgs& g, const TcContext& c, int M, int tiles_n, int K, i
   g.grid = g.groups * gs;
 }
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, bool RSPLIT>
 pds_status launch_impl(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t st,
                        std::string* err) {
   using Cf = Cfg<BN, PAIR>;
-  const void* fn = reinterpret_cast<const void*>(gemm_kernel<BN, EPI, PAIR>);
+  const void* fn = reinterpret_cast<const void*>(gemm_kernel<BN, EPI, PAIR, RSPLIT>);
   const cudaError_t attr_err = kernel_smem_attr(fn, static_cast<int>(Cf::kSmem));
   if (attr_err != cudaSuccess) {
     *err = std::string("gemm shared-memory attribute: ") + cudaGetErrorString(attr_err);
@@ -1842,7 +2055,23 @@ pds_status launch_impl(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStre
         }
       }
     }
-    if (g.cs > 1 && g.split < 2) {
+    if constexpr (RSPLIT) {
+      // every tile's cluster at once, or fewer CTAs per tile
+      int cc = g.rsplit;
+      while (cc >= 3 && fit(cc) < g.tiles_n) --cc;
+      if (cc != g.rsplit) {
+        if (cc >= 3) {
+          g.rsplit = cc;
+          g.cs = cc;
+          g.groups = g.tiles_n * cc;
+          g.grid = g.groups;
+        } else {
+          make_schedule(g, c, g.M, g.tiles_n, g.K, BN, kGemmMaxGrid, false, 0, false);
+          return launch_impl<BN, EPI, false, false>(c, maps, g, st, err);
+        }
+      }
+    }
+    if (g.cs > 1 && g.split < 2 && g.rsplit < 2) {
       const int cap_groups = std::max(1, fit(g.cs) * g.cs / g.gs);
       if (g.groups > cap_groups) {
         g.groups = cap_groups;
@@ -1865,7 +2094,7 @@ pds_status launch_impl(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStre
   cfg.gridDim = dim3(g.grid);
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t ce = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, EPI, PAIR>, maps, g);
+  cudaError_t ce = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, EPI, PAIR, RSPLIT>, maps, g);
   if (ce != cudaSuccess) {
     *err = std::string("gemm launch: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;
@@ -1877,9 +2106,10 @@ template <int BN, int EPI>
 pds_status launch(TcContext& c, const GemmMaps& maps, GemmArgs& g, cudaStream_t st,
                   std::string* err) {
   if constexpr (BN == 256) {
-    if (g.pair) return launch_impl<BN, EPI, true>(c, maps, g, st, err);
+    if (g.pair) return launch_impl<BN, EPI, true, false>(c, maps, g, st, err);
   }
-  return launch_impl<BN, EPI, false>(c, maps, g, st, err);
+  if (g.rsplit > 1) return launch_impl<BN, EPI, false, true>(c, maps, g, st, err);
+  return launch_impl<BN, EPI, false, false>(c, maps, g, st, err);
 }
 
 }  // namespace
@@ -2125,7 +2355,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   g.wrows0 = N;
   g.c_out = Cout;
   g.ldc = N;
-  make_schedule(g, c, M, N / kNoAllocBN, K, kNoAllocBN, grid_cap, false);
+  make_schedule(g, c, M, N / kNoAllocBN, K, kNoAllocBN, grid_cap, false, 0, false);
   g.cs = 1;  // a plain launch, without clusters
   GemmMaps maps{};
   if ((rc = get_map(c, &maps.a, A, K, M, err)) != PDS_OK) return rc;
@@ -2138,7 +2368,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
 
   using Cf = Cfg<kNoAllocBN, false>;
   const cudaError_t attr_err =
-      kernel_smem_attr(reinterpret_cast<const void*>(gemm_kernel<kNoAllocBN, kEpiPlain, false>),
+      kernel_smem_attr(reinterpret_cast<const void*>(gemm_kernel<kNoAllocBN, kEpiPlain, false, false>),
                        static_cast<int>(Cf::kSmem));
   if (attr_err != cudaSuccess) {
     *err = std::string("gemm shared-memory attribute: ") + cudaGetErrorString(attr_err);
@@ -2149,7 +2379,7 @@ pds_status tc_gemm_plain_noalloc(const uint16_t* A, const uint16_t* W, float* Co
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cf::kSmem;
   cfg.stream = st;
-  ce = cudaLaunchKernelEx(&cfg, gemm_kernel<kNoAllocBN, kEpiPlain, false>, maps, g);
+  ce = cudaLaunchKernelEx(&cfg, gemm_kernel<kNoAllocBN, kEpiPlain, false, false>, maps, g);
   if (ce != cudaSuccess) {
     *err = std::string("gemm launch: ") + cudaGetErrorString(ce);
     return PDS_ELAUNCH;

@@ -20,7 +20,13 @@ def _bf16(rng, *shape, scale=1.0):
 
 @pytest.mark.parametrize("M,N,K", [(8, 256, 64), (1, 128, 64), (130, 384, 320), (128, 512, 4096),
                                    (200, 640, 8192), (512, 5120, 3072), (2048, 3072, 2048),
-                                   (37, 128, 192)])
+                                   (37, 128, 192),
+                                   # one row tile over a cluster of c CTAs that finish row
+                                   # slices: c = 4 with a ragged last slice, c = 4 with three or
+                                   # two empty slices, c = 3 (48-row slices), c = 8 (16-row
+                                   # slices, 128-wide tiles), c = 6 (24-row slices)
+                                   (100, 768, 1024), (17, 128, 512), (64, 384, 512),
+                                   (9, 256, 384), (120, 384, 1024), (128, 640, 768)])
 def test_gemm_bf16_matches_fp64(M, N, K):
     from dense_decoder_layer_gb300 import pds
     rng = np.random.default_rng(M * 7 + N + K)

@@ -20,6 +20,10 @@ RAGGED = {
     # q|k|v = 384+128+128 columns: the last 256-column QKV tile is half empty;
     # d = 384 takes the 128-column residual tiles
     "odd-heads": synth.Dims(2, 384, 3, 1, 128, 768, 77, 9, 1.0e4),
+    # one row tile of 100 rows: every GEMM splits k over a cluster whose
+    # CTAs finish row slices (four of 32 rows, the last ragged; down: eight
+    # of 16 rows, the seventh ragged, the eighth empty)
+    "row-split": synth.Dims(2, 512, 8, 2, 64, 1536, 100, 20, 1.0e4),
 }
 
 
@@ -30,7 +34,8 @@ def _check(got, want, tag):
         assert_parity(got[2][l], want[2][l], f"{tag} v_rows[{l}]")
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged-hd64", "ragged-hd128", "single-row", "odd-heads"])
+@pytest.mark.parametrize("name", ["tiny", "ragged-hd64", "ragged-hd128", "single-row", "odd-heads",
+                                  "row-split"])
 def test_small_stacks_match_oracle(name):
     dims = RAGGED.get(name) or synth.CONFIGS[name]
     dims, (layers, pk, pv, hidden) = workload(dims)

@@ -34,6 +34,13 @@ CASES = {
     "everything": (HD64, synth.Variant(extras=True, rope_layout="norm", rot_dim=32,
                                        freq_factors=True, rope_mscale=1.1, attn_softcap=3.0,
                                        window=90)),
+    # the general QKV epilogue on one row tile whose k range is split over a
+    # cluster (row slices of 32: the last one ragged, or two of them empty)
+    "extras-hd128-row-split": (HD128.replace(batch=100), synth.Variant(extras=True)),
+    "everything-row-split": (HD64.replace(batch=60),
+                             synth.Variant(extras=True, rope_layout="norm", rot_dim=32,
+                                           freq_factors=True, rope_mscale=1.1,
+                                           attn_softcap=3.0, window=90)),
 }
 
 
