@@ -12,17 +12,20 @@
 //   warp 0      TMA producer: the Q tile once, then K and V tiles of 128
 //               keys (128-byte swizzle) into two-stage rings, K one ahead
 //   warp 1      tcgen05.mma issuer: S_j = Q K_j^T into one of two TMEM
-//               buffers, O += P_j V_j into a TMEM accumulator (V read
-//               MN-major straight from its cache layout)
+//               buffers, O += P_j V_j into a TMEM accumulator with P_j read
+//               from tensor memory (V read MN-major straight from its cache
+//               layout); the P.V MMA's completion frees the buffer
 //   warps 4-19  softmax, four threads per query row (TMEM lane), each with
 //               32 of the tile's keys: S_j from TMEM, causal mask, the row
 //               maximum (the quarters exchange theirs through shared
 //               memory), exp2 of the scaled score against the row's
-//               reference maximum, P_j as bf16 into shared memory (the A
-//               operand of the P.V MMA).  The reference maximum moves only
-//               when a row's maximum grows by more than 2^8 (the O row in
-//               TMEM is then rescaled once), so exp2 values stay <= 256.  At
-//               the end the quarters add their row sums in order and each
+//               reference maximum, P_j as bf16 pairs over the first columns
+//               of S_j's own buffer.  The reference maximum moves only when
+//               a row's maximum grows by more than 2^8 (the O row in TMEM is
+//               then rescaled once, after the previous P.V), so exp2 values
+//               stay <= 256 and the softmax never otherwise waits for the
+//               MMAs: it works on S_{j+1} while O += P_j V_j runs.  At the
+//               end the quarters add their row sums in order and each
 //               divides and stores a quarter of the O row.
 // S_{j+1} is computed while the softmax works on S_j.
 //
@@ -72,7 +75,7 @@ struct AttnCfg {
   static constexpr uint32_t kP0 = kV0 + 2u * kTile;  // one P buffer
   static constexpr uint32_t kX = kP0 + kP;           // row maxima / sums of the halves
   static constexpr uint32_t kBar = kX + 2u * kRowSplit * 128u * 4u;
-  static constexpr int kNumBars = 18;
+  static constexpr int kNumBars = 20;
   static constexpr size_t kSmem = 1024 + kBar + kNumBars * 8 + 16;
   static_assert(kSmem <= 232448, "shared memory per CTA");
   // TMEM: S buffers at columns 0 and 128, O at 256
@@ -221,9 +224,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto bar_v_full = [&](int st) { return bar0 + 8u * (5 + st); };
   auto bar_v_empty = [&](int st) { return bar0 + 8u * (7 + st); };
   auto bar_s_full = [&](int b) { return bar0 + 8u * (9 + b); };
+  // buffer b's S has been consumed: O += P V of the tile it held has completed
   auto bar_s_free = [&](int b) { return bar0 + 8u * (11 + b); };
-  const uint32_t bar_p_full = bar0 + 8u * 13;  // phase j: P_j is in shared memory
-  const uint32_t bar_pv = bar0 + 8u * 14;      // phase j: O += P_j V_j has completed
+  // per buffer b = j & 1, phase j >> 1: P_j is in tensor memory / O += P_j V_j
+  // has completed (one barrier per parity, so that a softmax warp a tile
+  // ahead of the MMAs never meets a phase of the tile after)
+  auto bar_p_full = [&](int b) { return bar0 + 8u * (b == 0 ? 13 : 18); };
+  auto bar_pv = [&](int b) { return bar0 + 8u * (b == 0 ? 14 : 19); };
   const uint32_t bar_drain = bar0 + 8u * 15;   // every MMA of the CTA has completed
   const uint32_t bar_m_ready = bar0 + 8u * 16;  // split, second CTA: the first may receive
   const uint32_t bar_m_recv = bar0 + 8u * 17;   // split, first CTA: the second's half landed
@@ -276,10 +283,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(bar_v_full(i), 1);
       mbar_init(bar_v_empty(i), 1);
       mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_s_free(i), kSoftmaxThreads / 32);  // one arrival per softmax warp
+      mbar_init(bar_s_free(i), 1);
+      mbar_init(bar_p_full(i), kSoftmaxThreads / 32);  // one arrival per softmax warp
+      mbar_init(bar_pv(i), 1);
     }
-    mbar_init(bar_p_full, kSoftmaxThreads / 32);
-    mbar_init(bar_pv, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_m_ready, 1);
     mbar_init(bar_m_recv, 1);
@@ -355,15 +362,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (j + 1 < n && !(ok = issue_s(j + 1))) break;
         const int st = j & 1;
         if (!(ok = mbar_wait(bar_v_full(st), (j >> 1) & 1, abort_flag, a.status))) break;
-        if (!(ok = mbar_wait(bar_p_full, j & 1, abort_flag, a.status))) break;
+        if (!(ok = mbar_wait(bar_p_full(st), (j >> 1) & 1, abort_flag, a.status))) break;
         tc_fence_after();
-        const uint32_t pb = sbase + C::kP0;
+        // P_j (bf16 pairs) sits over the first 64 columns of S_j's buffer
+        const uint32_t pt = tmem + st * 128u;
         const uint32_t vb = sbase + C::kV0 + st * C::kTile;
 #pragma unroll
         for (int k = 0; k < kKeys / 16; ++k)
-          umma_bf16(tm_o, kmajor_desc(pb, k), v_desc(vb, k), kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tm_o, pt + k * 8u, v_desc(vb, k), kIdPV, (j > 0 || k > 0) ? 1u : 0u);
         umma_commit(bar_v_empty(st));
-        umma_commit(bar_pv);
+        umma_commit(bar_pv(st));
+        umma_commit(bar_s_free(st));
       }
       umma_commit(bar_drain);
       int dummy = 0;
@@ -403,15 +412,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float sv[kPartKeys];
       float mx = -INFINITY;  // raw score maximum (the scale is positive)
       if (ok && !live) {
+        // P_j's phase still counts this warp (S_j's wait above keeps it
+        // within two tiles of the MMAs, as the live warps are)
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar_s_free(st));
-          mbar_arrive(bar_p_full);
-        }
-        // stay in step with the live warps: P_j's barrier phase completes only
-        // with their arrivals, so this warp's arrivals for tile j + 1 cannot
-        // count toward tile j's phases once O += P_j V_j has completed
-        wait(bar_pv, j & 1);
+        if (lane == 0) mbar_arrive(bar_p_full(st));
         continue;
       }
       if (ok) {
@@ -422,9 +426,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) sv[c * 32 + i] = t[i];
         }
+        // (P_j overwrites S_j's first columns once every part has read its
+        // keys: the row maximum's barrier below)
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_s_free(st));
         if (VAR && a.cap_raw > 0.f) {
           const float k2 = 2.0f * 1.4426950408889634f / a.cap_raw;
 #pragma unroll
@@ -448,6 +452,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // the row maximum: all parts
       xch[(st * kRowSplit + part) * 128 + r] = mx;
       named_bar_sync(1 + (warp & 3), 32 * kRowSplit);  // the warps of these 32 rows
+      tc_fence_after();
 #pragma unroll
       for (int q = 0; q < kRowSplit; ++q) mx = fmaxf(mx, xch[(st * kRowSplit + q) * 128 + r]);
       if (!ok) continue;
@@ -472,38 +477,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       const float sum = tree_sum<kPartKeys>(sv);
       l = l * alpha + sum;
-      if (j > 0) {
-        // O += P_{j-1} V_{j-1} has completed: O is stable and the P buffer free
-        wait(bar_pv, (j - 1) & 1);
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O must hold every earlier P V before it is scaled: the last one,
+        // O += P_{j-1} V_{j-1}, may still run (the ones before have completed:
+        // S_j's buffer was freed by O += P_{j-2} V_{j-2})
+        wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1);
         if (!ok) continue;
-        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-          for (int c = 0; c < kPartCols / 16; ++c) {
-            float t[16];
-            const uint32_t ta = tmem + lane_off + 256u + part * kPartCols + c * 16;
-            tmem_load16(ta, t);
+        for (int c = 0; c < kPartCols / 16; ++c) {
+          float t[16];
+          const uint32_t ta = tmem + lane_off + 256u + part * kPartCols + c * 16;
+          tmem_load16(ta, t);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) t[i] *= alpha;
-            tmem_store16(ta, t);
-          }
+          for (int i = 0; i < 16; ++i) t[i] *= alpha;
+          tmem_store16(ta, t);
         }
       }
-      // P row r, keys of this part: 64-key blocks of 16 KB, 128 bytes per
-      // row, 16-byte chunks swizzled by the row
-      const int kfirst = part * kPartKeys;
-      const uint32_t prow = sbase + C::kP0 + static_cast<uint32_t>(kfirst >> 6) * 16384u +
-                            static_cast<uint32_t>(r) * 128u;
-      const uint32_t sw = static_cast<uint32_t>(r & 7);
+      // P row r, keys of this part: bf16 pairs into columns 16 part .. 16 part
+      // + 15 of S_j's buffer (the A operand of O += P_j V_j)
+      {
+        float pw[kPartKeys / 2];
 #pragma unroll
-      for (int c = 0; c < kPartKeys / 8; ++c)
-        *reinterpret_cast<uint4*>(
-            smem + (prow - sbase) +
-            ((static_cast<uint32_t>(((kfirst & 63) >> 3) + c) ^ sw) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
+        for (int i = 0; i < kPartKeys / 2; ++i) pw[i] = __uint_as_float(pk[i]);
+        tmem_store16_nowait(tmem + lane_off + st * 128u + part * (kPartKeys / 2), pw);
+        tmem_wait_st();
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full);
+      if (lane == 0) mbar_arrive(bar_p_full(st));
     }
     // the row sum of all parts (in part order), while the last P.V runs;
     // then O row / l
@@ -514,7 +515,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       l = 0.f;
 #pragma unroll
       for (int q = 0; q < kRowSplit; ++q) l += xch[q * 128 + r];
-      wait(bar_pv, (n - 1) & 1);
+      wait(bar_pv((n - 1) & 1), ((n - 1) >> 1) & 1);
     }
     // split: the second CTA's O part (float32, 16-byte chunks swizzled by the
     // row) goes to the first CTA at the K stages' offset, its row sum and

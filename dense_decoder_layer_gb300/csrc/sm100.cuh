@@ -290,6 +290,19 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, one 128 x N x 16 step with A read from
+// tensor memory (row i in lane i, two 16-bit elements per 32-bit column, the
+// lower k in the low half).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // CTA-pair MMA (cta_group::2), issued by the even CTA of the pair: a
 // 256 x N x 16 step whose A rows 0..127 and B rows 0..N/2-1 sit in this
 // CTA's shared memory and A rows 128..255 and B rows N/2..N-1 at the same
