@@ -94,7 +94,7 @@ def algo_bytes(dims):
 
 
 KERNEL_SOURCES = ("gemm_tc.cu", "sm100.cuh", "attn_tc.cu", "prep.cu", "tc.h", "kernels.h",
-                  "common.cuh")
+                  "common.cuh", "fastmath.cuh")
 
 
 def kernel_source_sha():

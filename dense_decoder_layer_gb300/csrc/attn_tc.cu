@@ -11,7 +11,7 @@
 // One CTA per (query head, 128 query rows), heaviest row tiles first.
 //   warp 0      TMA producer: the Q tile once, then K and V tiles of 128
 //               keys (128-byte swizzle) into two-stage rings, K one ahead
-//   warp 1      tcgen05.mma issuer: S_j = Q K_j^T into one of two TMEM
+//   warp 1      tcgen05.mma issuer: S_j = Q K_j^T into one of three TMEM
 //               buffers, O += P_j V_j into a TMEM accumulator with P_j read
 //               from tensor memory (V read MN-major straight from its cache
 //               layout); the P.V MMA's completion frees the buffer
@@ -27,7 +27,9 @@
 //               MMAs: it works on S_{j+1} while O += P_j V_j runs.  At the
 //               end the quarters add their row sums in order and each
 //               divides and stores a quarter of the O row.
-// S_{j+1} is computed while the softmax works on S_j.
+// S_{j+1} is computed while the softmax works on S_j; with three buffers the
+// MMA issuer never waits for O += P_{j-1} V_{j-1} to finish before issuing
+// S_{j+1}, so the tensor pipe runs S and P.V back to back.
 //
 // Key-range split: when there are fewer query tiles than SMs, the heaviest
 // tiles with long key ranges (as many as fit one CTA per SM) are computed by
@@ -45,6 +47,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "fastmath.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
 #include "tc.h"
@@ -68,17 +71,25 @@ constexpr int kSplitMinKeyTiles = 8;
 template <int HD>
 struct AttnCfg {
   static constexpr uint32_t kTile = 128u * HD * 2u;  // Q, K or V tile (bf16)
-  static constexpr uint32_t kP = 128u * kKeys * 2u;  // P tile (bf16)
+  // K and V rings: a stage is reloaded only once the MMA that reads it has
+  // completed, so a ring of S stages hides a load latency of about S - 1
+  // tile times (an L2-resident tile takes ~1.2 us to land)
+  static constexpr int kKStages = HD == 128 ? 2 : 3;
+  static constexpr int kVStages = 3;
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK0 = kTile;             // K stage s at kK0 + s kTile
-  static constexpr uint32_t kV0 = kK0 + 2u * kTile;  // V stage s at kV0 + s kTile
-  static constexpr uint32_t kP0 = kV0 + 2u * kTile;  // one P buffer
-  static constexpr uint32_t kX = kP0 + kP;           // row maxima / sums of the halves
+  static constexpr uint32_t kK0 = kTile;                     // K stage s at kK0 + s kTile
+  static constexpr uint32_t kV0 = kK0 + kKStages * kTile;    // V stage s at kV0 + s kTile
+  static constexpr uint32_t kP0 = kV0 + kVStages * kTile;    // split: the second half's (l, m)
+  static constexpr uint32_t kX = kP0 + 1024u;                // row maxima / sums of the halves
   static constexpr uint32_t kBar = kX + 2u * kRowSplit * 128u * 4u;
-  static constexpr int kNumBars = 20;
+  static constexpr int kNumBars = 28;
   static constexpr size_t kSmem = 1024 + kBar + kNumBars * 8 + 16;
   static_assert(kSmem <= 232448, "shared memory per CTA");
-  // TMEM: S buffers at columns 0 and 128, O at 256
+  // the split's second half sends its float32 O rows into the K stages
+  static_assert(kKStages * kTile >= 128u * HD * 4u, "the O of a split half fits the K stages");
+  // TMEM: three S (then P) buffers at columns 0, 128 and 256, O at 384
+  static constexpr int kSBufs = 3;
+  static constexpr uint32_t kTmO = 384;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -183,21 +194,25 @@ __device__ __forceinline__ uint64_t v_desc(uint32_t base, int kstep) {
 __device__ __forceinline__ float exp2_sfu(float x) { return exp2_sfu_raw(x); }
 
 // Pairwise (tree) maximum and sum of n values.
-template <int N>
-__device__ __forceinline__ float tree_max(const float* v) {
-  if constexpr (N == 1) {
-    return v[0];
-  } else {
-    return fmaxf(tree_max<N / 2>(v), tree_max<N / 2>(v + N / 2));
-  }
+// Maximum of 32 values by three-input maxima (16 instructions).
+__device__ __forceinline__ float max32(const float* v) {
+  float a[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[10] = fmaxf(v[30], v[31]);
+  const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]);
+  const float b2 = max3(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+  return fmaxf(max3(b0, b1, b2), b3);
 }
-template <int N>
-__device__ __forceinline__ float tree_sum(const float* v) {
-  if constexpr (N == 1) {
-    return v[0];
-  } else {
-    return tree_sum<N / 2>(v) + tree_sum<N / 2>(v + N / 2);
+// Sum of 32 values in a fixed pairwise order, two lanes per instruction
+// (the values are consumed).
+__device__ __forceinline__ float sum32(float* v) {
+#pragma unroll
+  for (int w = 16; w >= 2; w >>= 1) {
+#pragma unroll
+    for (int k = 0; k < w / 2; ++k) add2(v[2 * k], v[2 * k + 1], v[2 * k + w], v[2 * k + w + 1]);
   }
+  return v[0] + v[1];
 }
 
 // kind::f16 instruction descriptor: bf16 x bf16 -> f32, M x N, B MN-major if b_mn.
@@ -219,21 +234,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = smem_raw + (sbase - raw);
   const uint32_t bar0 = sbase + C::kBar;
   const uint32_t bar_q = bar0;
+  // ring stages (at most 3 of each)
   auto bar_k_full = [&](int st) { return bar0 + 8u * (1 + st); };
-  auto bar_k_empty = [&](int st) { return bar0 + 8u * (3 + st); };
-  auto bar_v_full = [&](int st) { return bar0 + 8u * (5 + st); };
-  auto bar_v_empty = [&](int st) { return bar0 + 8u * (7 + st); };
-  auto bar_s_full = [&](int b) { return bar0 + 8u * (9 + b); };
-  // buffer b's S has been consumed: O += P V of the tile it held has completed
-  auto bar_s_free = [&](int b) { return bar0 + 8u * (11 + b); };
-  // per buffer b = j & 1, phase j >> 1: P_j is in tensor memory / O += P_j V_j
-  // has completed (one barrier per parity, so that a softmax warp a tile
-  // ahead of the MMAs never meets a phase of the tile after)
-  auto bar_p_full = [&](int b) { return bar0 + 8u * (b == 0 ? 13 : 18); };
-  auto bar_pv = [&](int b) { return bar0 + 8u * (b == 0 ? 14 : 19); };
-  const uint32_t bar_drain = bar0 + 8u * 15;   // every MMA of the CTA has completed
-  const uint32_t bar_m_ready = bar0 + 8u * 16;  // split, second CTA: the first may receive
-  const uint32_t bar_m_recv = bar0 + 8u * 17;   // split, first CTA: the second's half landed
+  auto bar_k_empty = [&](int st) { return bar0 + 8u * (4 + st); };
+  auto bar_v_full = [&](int st) { return bar0 + 8u * (7 + st); };
+  auto bar_v_empty = [&](int st) { return bar0 + 8u * (10 + st); };
+  // Per TMEM buffer b = j % 3, phase (j / 3) & 1: S_j is in it / it is free
+  // again (O += P V of the tile it held has completed) / P_j is in it /
+  // O += P_j V_j has completed.  A barrier per buffer keeps every wait within
+  // one phase: a softmax warp is at most two tiles ahead of the P.V MMAs.
+  auto bar_s_full = [&](int b) { return bar0 + 8u * (13 + b); };
+  auto bar_s_free = [&](int b) { return bar0 + 8u * (16 + b); };
+  auto bar_p_full = [&](int b) { return bar0 + 8u * (19 + b); };
+  auto bar_pv = [&](int b) { return bar0 + 8u * (22 + b); };
+  const uint32_t bar_drain = bar0 + 8u * 25;   // every MMA of the CTA has completed
+  const uint32_t bar_m_ready = bar0 + 8u * 26;  // split, second CTA: the first may receive
+  const uint32_t bar_m_recv = bar0 + 8u * 27;   // split, first CTA: the second's half landed
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kBar + C::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
@@ -277,11 +293,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(bar_k_full(i), 1);
       mbar_init(bar_k_empty(i), 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
       mbar_init(bar_v_full(i), 1);
       mbar_init(bar_v_empty(i), 1);
+    }
+    for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(bar_s_full(i), 1);
       mbar_init(bar_s_free(i), 1);
       mbar_init(bar_p_full(i), kSoftmaxThreads / 32);  // one arrival per softmax warp
@@ -317,62 +337,83 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_arrive_expect_tx(bar_q, C::kTile);
       for (int c = 0; c < HD / 64; ++c)
         tma_load_2d(sbase + C::kQ + c * 16384u, &maps.q, bar_q, h * HD + c * 64, b0, pol);
-      // K_j is freed by S_j, V_j by O += P_j V_j, which comes later: K
-      // runs one tile ahead of V (K_0, K_1, V_0, K_2, V_1, ...)
-      auto load = [&](const CUtensorMap* map, uint32_t base, uint32_t full, uint32_t empty, int j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(empty + 8u * st, ((j >> 1) - 1) & 1, abort_flag, a.status))
-          return false;
+      // K_j is freed by S_j, V_j by O += P_j V_j, which comes later.  Each
+      // load goes out as soon as its stage is free, K and V independently
+      // (neither waits behind the other).
+      auto issue = [&](const CUtensorMap* map, uint32_t base, uint32_t full, int st, int j) {
         mbar_arrive_expect_tx(full + 8u * st, C::kTile);
         for (int c = 0; c < HD / 64; ++c)
           tma_load_2d(base + st * C::kTile + c * 16384u, map, full + 8u * st, g * HD + c * 64,
                       (kt0 + j) * kKeys, pol);
-        return true;
       };
-      bool ok = load(&maps.k, sbase + C::kK0, bar_k_full(0), bar_k_empty(0), 0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n && !(ok = load(&maps.k, sbase + C::kK0, bar_k_full(0), bar_k_empty(0), j + 1)))
-          break;
-        ok = load(&maps.v, sbase + C::kV0, bar_v_full(0), bar_v_empty(0), j);
+      auto stage_free = [&](uint32_t empty, int stages, int j) {
+        return j < stages || mbar_try_wait(empty + 8u * (j % stages), ((j / stages) - 1) & 1);
+      };
+      int kj = 0, vj = 0;
+      const uint64_t t0 = global_timer_ns();
+      uint32_t idle = 0;
+      while (kj < n || vj < n) {
+        bool progress = false;
+        if (kj < n && stage_free(bar_k_empty(0), C::kKStages, kj)) {
+          issue(&maps.k, sbase + C::kK0, bar_k_full(0), kj % C::kKStages, kj);
+          ++kj;
+          progress = true;
+        }
+        if (vj < kj && stage_free(bar_v_empty(0), C::kVStages, vj)) {
+          issue(&maps.v, sbase + C::kV0, bar_v_full(0), vj % C::kVStages, vj);
+          ++vj;
+          progress = true;
+        }
+        // bounded as the mbarrier waits are: give up after their limit, or
+        // as soon as another role of the CTA has given up
+        if (!progress && (++idle & 63u) == 0) {
+          if (*abort_flag) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(a.status, kStatusTimeout);
+            break;
+          }
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_attn(128, kKeys, false);
       constexpr uint32_t kIdPV = idesc_attn(128, HD, true);
-      const uint32_t tm_o = tmem + 256;
+      const uint32_t tm_o = tmem + C::kTmO;
       bool ok = mbar_wait(bar_q, 0, abort_flag, a.status);
       auto issue_s = [&](int j) {
-        const int st = j & 1;
-        if (!mbar_wait(bar_k_full(st), (j >> 1) & 1, abort_flag, a.status)) return false;
-        if (j >= 2 && !mbar_wait(bar_s_free(st), ((j >> 1) - 1) & 1, abort_flag, a.status))
+        const int st = j % C::kKStages, sb = j % C::kSBufs;  // K stage, S buffer
+        if (!mbar_wait(bar_k_full(st), (j / C::kKStages) & 1, abort_flag, a.status)) return false;
+        if (j >= C::kSBufs &&
+            !mbar_wait(bar_s_free(sb), ((j / C::kSBufs) - 1) & 1, abort_flag, a.status))
           return false;
         tc_fence_after();
         const uint32_t kb = sbase + C::kK0 + st * C::kTile;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          umma_bf16(tmem + st * 128u, kmajor_desc(sbase + C::kQ, k), kmajor_desc(kb, k), kIdS,
+          umma_bf16(tmem + sb * 128u, kmajor_desc(sbase + C::kQ, k), kmajor_desc(kb, k), kIdS,
                     k > 0 ? 1u : 0u);
-        umma_commit(bar_s_full(st));
+        umma_commit(bar_s_full(sb));
         umma_commit(bar_k_empty(st));
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n && !(ok = issue_s(j + 1))) break;
-        const int st = j & 1;
-        if (!(ok = mbar_wait(bar_v_full(st), (j >> 1) & 1, abort_flag, a.status))) break;
-        if (!(ok = mbar_wait(bar_p_full(st), (j >> 1) & 1, abort_flag, a.status))) break;
+        const int st = j % C::kVStages, sb = j % C::kSBufs;  // V stage, S / P buffer
+        if (!(ok = mbar_wait(bar_v_full(st), (j / C::kVStages) & 1, abort_flag, a.status))) break;
+        if (!(ok = mbar_wait(bar_p_full(sb), (j / C::kSBufs) & 1, abort_flag, a.status))) break;
         tc_fence_after();
         // P_j (bf16 pairs) sits over the first 64 columns of S_j's buffer
-        const uint32_t pt = tmem + st * 128u;
+        const uint32_t pt = tmem + sb * 128u;
         const uint32_t vb = sbase + C::kV0 + st * C::kTile;
 #pragma unroll
         for (int k = 0; k < kKeys / 16; ++k)
           umma_bf16_ts(tm_o, pt + k * 8u, v_desc(vb, k), kIdPV, (j > 0 || k > 0) ? 1u : 0u);
         umma_commit(bar_v_empty(st));
-        umma_commit(bar_pv(st));
-        umma_commit(bar_s_free(st));
+        umma_commit(bar_pv(sb));
+        umma_commit(bar_s_free(sb));
       }
       umma_commit(bar_drain);
       int dummy = 0;
@@ -388,7 +429,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the row's position less the first key of this part of key tile 0
     const int rel0 = a.s + b0 + r - (kt0 * kKeys + part * kPartKeys);
     constexpr int kPartCols = HD / kRowSplit;
-    static_assert(kPartKeys % 32 == 0 && kPartCols % 16 == 0, "TMEM loads of the parts");
+    static_assert(kPartKeys == 32 && kPartCols % 16 == 0, "TMEM loads and reductions of the parts");
     const float sc = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;  // m_ref in scaled (base-2) units
     // Every softmax thread passes the named barriers of every tile, even
@@ -407,22 +448,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // rows, so they are live or dead together.
     const bool live = b0 + (sw_idx & 3) * 32 < a.B;
     for (int j = 0; j < n; ++j) {
-      const int st = j & 1;
-      wait(bar_s_full(st), (j >> 1) & 1);
+      const int st = j & 1, sb = j % C::kSBufs;  // exchange slot, S / P buffer
+      wait(bar_s_full(sb), (j / C::kSBufs) & 1);
       float sv[kPartKeys];
       float mx = -INFINITY;  // raw score maximum (the scale is positive)
       if (ok && !live) {
         // P_j's phase still counts this warp (S_j's wait above keeps it
         // within two tiles of the MMAs, as the live warps are)
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_p_full(st));
+        if (lane == 0) mbar_arrive(bar_p_full(sb));
         continue;
       }
       if (ok) {
 #pragma unroll
         for (int c = 0; c < kPartKeys / 32; ++c) {
           float t[32];
-          tmem_load32(tmem + lane_off + st * 128u + part * kPartKeys + c * 32, t);
+          tmem_load32(tmem + lane_off + sb * 128u + part * kPartKeys + c * 32, t);
 #pragma unroll
           for (int i = 0; i < 32; ++i) sv[c * 32 + i] = t[i];
         }
@@ -447,7 +488,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int i = 0; i < kPartKeys; ++i)
             if (i <= lo) sv[i] = -INFINITY;
         }
-        mx = tree_max<kPartKeys>(sv);
+        mx = max32(sv);
       }
       // the row maximum: all parts
       xch[(st * kRowSplit + part) * 128 + r] = mx;
@@ -470,23 +511,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint32_t pk[kPartKeys / 2];
       const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // masked scores give 0
 #pragma unroll
-      for (int i = 0; i < kPartKeys / 2; ++i) {
-        sv[2 * i] = exp2_sfu(fmaf(sv[2 * i], sc, -m_use));
-        sv[2 * i + 1] = exp2_sfu(fmaf(sv[2 * i + 1], sc, -m_use));
-        pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
-      }
-      const float sum = tree_sum<kPartKeys>(sv);
+      for (int i = 0; i < kPartKeys / 2; ++i) fma2(sv[2 * i], sv[2 * i + 1], sc, -m_use);
+#pragma unroll
+      for (int i = 0; i < kPartKeys; ++i) sv[i] = exp2_sfu(sv[i]);
+#pragma unroll
+      for (int i = 0; i < kPartKeys / 2; ++i) pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+      const float sum = sum32(sv);
       l = l * alpha + sum;
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O must hold every earlier P V before it is scaled: the last one,
-        // O += P_{j-1} V_{j-1}, may still run (the ones before have completed:
-        // S_j's buffer was freed by O += P_{j-2} V_{j-2})
-        wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1);
+        // O must hold every earlier P V before it is scaled: the last two may
+        // still run; they complete in order, so the wait is for the last
+        wait(bar_pv((j - 1) % C::kSBufs), ((j - 1) / C::kSBufs) & 1);
         if (!ok) continue;
 #pragma unroll
         for (int c = 0; c < kPartCols / 16; ++c) {
           float t[16];
-          const uint32_t ta = tmem + lane_off + 256u + part * kPartCols + c * 16;
+          const uint32_t ta = tmem + lane_off + C::kTmO + part * kPartCols + c * 16;
           tmem_load16(ta, t);
 #pragma unroll
           for (int i = 0; i < 16; ++i) t[i] *= alpha;
@@ -499,12 +539,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float pw[kPartKeys / 2];
 #pragma unroll
         for (int i = 0; i < kPartKeys / 2; ++i) pw[i] = __uint_as_float(pk[i]);
-        tmem_store16_nowait(tmem + lane_off + st * 128u + part * (kPartKeys / 2), pw);
+        tmem_store16_nowait(tmem + lane_off + sb * 128u + part * (kPartKeys / 2), pw);
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full(st));
+      if (lane == 0) mbar_arrive(bar_p_full(sb));
     }
     // the row sum of all parts (in part order), while the last P.V runs;
     // then O row / l
@@ -515,7 +555,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       l = 0.f;
 #pragma unroll
       for (int q = 0; q < kRowSplit; ++q) l += xch[q * 128 + r];
-      wait(bar_pv((n - 1) & 1), ((n - 1) >> 1) & 1);
+      wait(bar_pv((n - 1) % C::kSBufs), ((n - 1) / C::kSBufs) & 1);
     }
     // split: the second CTA's O part (float32, 16-byte chunks swizzled by the
     // row) goes to the first CTA at the K stages' offset, its row sum and
@@ -533,7 +573,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < kPartCols / 16; ++c) {
           float t[16];
-          tmem_load16(tmem + lane_off + 256u + part * kPartCols + c * 16, t);
+          tmem_load16(tmem + lane_off + C::kTmO + part * kPartCols + c * 16, t);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             __stcg(reinterpret_cast<float4*>(dst + c * 16) + i,
@@ -547,7 +587,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < kPartCols / 16; ++c) {
           float t[16];
-          tmem_load16(tmem + lane_off + 256u + part * kPartCols + c * 16, t);
+          tmem_load16(tmem + lane_off + C::kTmO + part * kPartCols + c * 16, t);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             *reinterpret_cast<float4*>(smem + o_chunk(4 * c + i)) =
@@ -591,7 +631,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < kPartCols / 16; ++c) {
           float t[16];
-          tmem_load16(tmem + lane_off + 256u + part * kPartCols + c * 16, t);
+          tmem_load16(tmem + lane_off + C::kTmO + part * kPartCols + c * 16, t);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float4 o1 = *reinterpret_cast<const float4*>(smem + o_chunk(4 * c + i));
@@ -618,7 +658,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
       for (int c = 0; c < kPartCols / 16; ++c) {
         float t[16];
-        tmem_load16(tmem + lane_off + 256u + part * kPartCols + c * 16, t);
+        tmem_load16(tmem + lane_off + C::kTmO + part * kPartCols + c * 16, t);
         if (b < a.B) {
 #pragma unroll
           for (int i = 0; i < 2; ++i)
