@@ -1071,12 +1071,16 @@ __host__ __device__ __forceinline__ int rsplit_rows(int c) { return ((BM + c - 1
 //     other CTA's slice into that CTA's drained stages, laid out
 //     [contributor t][chunk][row of the slice][128 bytes].  The received
 //     slices and the outgoing boxes share the drained stages, none reused.
-//  2. Once its own slices have landed, the warps that hold the slice's rows
-//     in TMEM add the contributions in k order (cluster rank order, from
-//     zero, its own in its place), a 32-column chunk at a time with each
-//     contributor's 32 values loaded at once, and write the sums back to
-//     TMEM for the epilogue.
-// Returns false if a wait gave up.
+//  2. Once its own slices have landed, all epilogue threads fold them, each
+//     16-byte piece of the slice by one thread, into the sum of the ranks
+//     before this CTA's and the sum of those after it (each in rank order,
+//     from zero), written over contributor slots 0 and c - 2.
+//  3. The warps that hold the slice's rows in TMEM make (before + own) +
+//     after and write it back to TMEM for the epilogue.
+// The order of the additions is fixed, so the result does not depend on
+// timing.  Every epilogue thread reaches the barrier between 2 and 3, and
+// all leave on the abort flag after it, so a wait that gives up cannot
+// split the CTA.  Returns false if a wait gave up.
 template <int BN, int EPI>
 __device__ __forceinline__ bool rsplit_exchange(const GemmArgs& g, uint32_t taddr, int row, int ch,
                                                 int lane, uint8_t* sm, uint32_t sbase,
@@ -1087,20 +1091,22 @@ __device__ __forceinline__ bool rsplit_exchange(const GemmArgs& g, uint32_t tadd
   constexpr int kChunks = BN / 32;
   const int c = g.rsplit, R = rsplit_rows(c);
   const int lo = me * R, hs = lo + R, hi = min(g.M, hs);  // the rows this CTA finishes
+  const int n = max(0, hi - lo);
   auto recv_off = [&](int t, int j, int r) {
     return static_cast<uint32_t>(((t * kChunks + j) * R + r) * 128);
   };
-  const uint32_t recv_bytes = static_cast<uint32_t>((c - 1) * R * BN * 4);
+  const uint32_t slot_bytes = static_cast<uint32_t>(kChunks * R * 128);  // one contributor's
+  const uint32_t recv_bytes = static_cast<uint32_t>(c - 1) * slot_bytes;
   if (leader) {
-    mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>((c - 1) * max(0, hi - lo) * BN * 4));
+    mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>((c - 1) * n * BN * 4));
     for (int p = 0; p < c; ++p)
       if (p != me) mbar_arrive_cluster(mapa_shared(bar_ready, static_cast<uint32_t>(p)));
   }
-  if (!mbar_wait(bar_ready, 0, abort_flag, g.status)) return false;
-  tc_fence_after();
+  bool ok = __all_sync(0xffffffffu, mbar_wait(bar_ready, 0, abort_flag, g.status));
   const int w0 = row & ~31, lg = w0 / 32;  // this warp's rows w0 .. w0 + 31
   const uint32_t sw = static_cast<uint32_t>(row & 7);
-  {
+  if (ok) {
+    tc_fence_after();
     // lane group l holds rows of other slices that exist
     auto sends_of = [&](int l) {
       return 32 * l < g.M && (32 * l < lo || min(32 * l + 32, g.M) > hs);
@@ -1138,10 +1144,45 @@ __device__ __forceinline__ bool rsplit_exchange(const GemmArgs& g, uint32_t tadd
         }
       }
     }
+    ok = __all_sync(0xffffffffu, mbar_wait(bar_recv, 0, abort_flag, g.status));
   }
-  if (!mbar_wait(bar_recv, 0, abort_flag, g.status)) return false;
-  // TMEM accesses are warp-wide: a warp holding any finished row takes part
-  if (w0 >= hi || w0 + 32 <= lo) return true;
+  // 2. before / after sums of the received slices, one 16-byte piece a thread
+  const uint32_t before = sbase, after = sbase + static_cast<uint32_t>(me > 0 ? c - 2 : 0) * slot_bytes;
+  if (ok) {
+    const int et = static_cast<int>(threadIdx.x) - kEpiFirstThread;
+#pragma unroll 1
+    for (int idx = et; idx < kChunks * n * 8; idx += kEpiThreads) {
+      const int q4 = idx & 7, rest = idx >> 3, r = rest % n, j = rest / n;
+      const uint32_t off = recv_off(0, j, r) + ((static_cast<uint32_t>(q4) ^ (r & 7)) << 4);
+      // all contributors' pieces in flight at once (c - 1 <= 7), then the
+      // two sums in rank order
+      float4 x[7];
+#pragma unroll
+      for (int t = 0; t < 7; ++t)
+        if (t < c - 1) x[t] = *sm_at<float4>(sm, sbase, sbase + static_cast<uint32_t>(t) * slot_bytes + off);
+      float4 pre = make_float4(0.f, 0.f, 0.f, 0.f), post = pre;
+#pragma unroll
+      for (int t = 0; t < 7; ++t) {
+        if (t < me) {
+          pre.x += x[t].x;
+          pre.y += x[t].y;
+          pre.z += x[t].z;
+          pre.w += x[t].w;
+        } else if (t < c - 1) {
+          post.x += x[t].x;
+          post.y += x[t].y;
+          post.z += x[t].z;
+          post.w += x[t].w;
+        }
+      }
+      if (me > 0) *sm_at<float4>(sm, sbase, before + off) = pre;
+      if (me < c - 1) *sm_at<float4>(sm, sbase, after + off) = post;
+    }
+  }
+  named_bar_sync(1, kEpiThreads);
+  if (*abort_flag) return false;
+  // 3. (before + own) + after, by the warps that hold the slice's rows
+  if (n == 0 || w0 >= hi || w0 + 32 <= lo) return true;
   const bool mine = row >= lo && row < hi;
   const int r = mine ? row - lo : 0;
 #pragma unroll 1
@@ -1150,32 +1191,29 @@ __device__ __forceinline__ bool rsplit_exchange(const GemmArgs& g, uint32_t tadd
     float own[32];
     tmem_load32(taddr + j * 32, own);
     if (mine) {
-      float v[32];
+      const uint32_t roff = recv_off(0, j, r);
+      if (me > 0) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = 0.f;
-#pragma unroll 1
-      for (int p = 0; p < c; ++p) {
-        if (p == me) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] += own[e];
-        } else {
-          // the contributor's 32 values, all eight loads in flight at once
-          const uint32_t base = sbase + recv_off(p < me ? p : p - 1, j, r);
-          float4 x[8];
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            x[q4] = *sm_at<float4>(sm, sbase, base + ((static_cast<uint32_t>(q4) ^ sw) << 4));
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            v[4 * q4] += x[q4].x;
-            v[4 * q4 + 1] += x[q4].y;
-            v[4 * q4 + 2] += x[q4].z;
-            v[4 * q4 + 3] += x[q4].w;
-          }
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 x =
+              *sm_at<float4>(sm, sbase, before + roff + ((static_cast<uint32_t>(q4) ^ sw) << 4));
+          own[4 * q4] = x.x + own[4 * q4];
+          own[4 * q4 + 1] = x.y + own[4 * q4 + 1];
+          own[4 * q4 + 2] = x.z + own[4 * q4 + 2];
+          own[4 * q4 + 3] = x.w + own[4 * q4 + 3];
         }
       }
+      if (me < c - 1) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) own[e] = v[e];
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 x =
+              *sm_at<float4>(sm, sbase, after + roff + ((static_cast<uint32_t>(q4) ^ sw) << 4));
+          own[4 * q4] += x.x;
+          own[4 * q4 + 1] += x.y;
+          own[4 * q4 + 2] += x.z;
+          own[4 * q4 + 3] += x.w;
+        }
+      }
     }
     tmem_store16_nowait(taddr + j * 32, reinterpret_cast<const float(&)[16]>(own[0]));
     tmem_store16_nowait(taddr + j * 32 + 16, reinterpret_cast<const float(&)[16]>(own[16]));
