@@ -383,17 +383,6 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Atomic add at GPU scope with acquire-release semantics: after a CTA
-// barrier, one thread's call publishes the CTA's earlier writes and, with a
-// barrier after it, makes other CTAs' writes published the same way visible
-// to the whole CTA.
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
-
 // 16 consecutive columns of this thread's lane from registers; waits until
 // the stores are done.
 __device__ __forceinline__ void tmem_store16(uint32_t taddr, const float (&v)[16]) {
@@ -442,29 +431,6 @@ __device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 8 consecutive float32 columns of this thread's TMEM lane, waiting for the load.
-__device__ __forceinline__ void tmem_load8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-// 8 consecutive columns of this thread's lane from registers, without waiting.
-__device__ __forceinline__ void tmem_store8_nowait(uint32_t taddr, const float (&v)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
-      : "memory");
 }
 
 // Two 16-column TMEM loads (this thread's lane) with a single wait.
